@@ -1,0 +1,364 @@
+"""Benchmark of the fused FlashAdamW step on the Llama-3-8B tensor list.
+
+One step = one ``fo_adamw_step`` call (one kernel launch) over all 291
+parameter tensors (8,030,261,248 parameters): bf16 theta' + int8 rho (24-bit
+master), int8 / uint8 m and v codes with fp16 group-32 scales, bf16 grads.
+Inputs are synthetic (seeded N(0, 0.02) weights, N(0, 1e-3) grads) and far
+larger than L2 (98 GB move per step), so no L2 flush is needed.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the slow, literal CPU statement of the method) on a bounded sample of
+the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) for fused AdamW step"
+UNIT = "params/s"
+MODEL = W.LLAMA3_8B
+HYPER = W.LLAMA3_8B_HYPER
+MASTER_BITS = W.LLAMA3_8B_MASTER_BITS
+RHO_BITS = 8 if MASTER_BITS == 24 else 16
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_config(numels) -> dict:
+    return {
+        "workload": (f"{MODEL.name} tensor list: {len(numels)} tensors, {sum(numels):,} params; "
+                     f"bf16 theta' + int{RHO_BITS} rho ({MASTER_BITS}-bit master), int8/uint8 m/v codes "
+                     "+ fp16 group-32 scales, bf16 grads; lr 3e-4, betas (0.9, 0.95), eps 1e-8, wd 0.1"),
+        "params": int(sum(numels)),
+        "tensors": len(numels),
+        "l2": "inputs larger than L2 (no flush needed)",
+    }
+
+
+def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
+    """Bytes the step must move: read grad, theta', rho, m/v codes and scales;
+    write theta', rho, m/v codes and scales (12.25 B/param for bf16 grad + int8 rho)."""
+    total = 0
+    for n in numels:
+        g = (n + 31) // 32
+        total += n * (grad_bytes + 2 * 2 + 2 * rho_bytes + 2 * 1 + 2 * 1) + 2 * 2 * (2 * g)
+    return total
+
+
+def load_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines: list[str] = []
+        ident = None
+        try:
+            ident = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+        self.ident = ident if ident else str(device_index)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self) -> dict | None:
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ GPU arm
+def build_state(device):
+    from quantized_state_optimizer_gb300.optim import FlashAdamWState
+    specs = W.llama_tensor_list(MODEL)
+    numels = [s.numel for s in specs]
+    wid = W.WORKLOAD_IDS[MODEL.name]
+    st = FlashAdamWState(numels, rho_bits=RHO_BITS, grad_dtype=torch.bfloat16, device=device)
+    for i, s in enumerate(specs):
+        st.init_theta(i, W.init_theta(s, wid, i, device))
+        W.make_grad(s.numel, wid, i, 1, device, out=st.grad_view(i))
+    torch.cuda.synchronize()
+    return st, numels
+
+
+def time_steps(st, steps: int, warmup: int, stream, dist_on: bool) -> tuple[float, list[float]]:
+    h = HYPER
+    t = 0
+    for _ in range(warmup):
+        t += 1
+        st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        t += 1
+        starts[k].record(stream)
+        st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, stream=stream)
+        ends[k].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return total_ms, per
+
+
+def time_e2e(st, numels, steps: int, stream) -> dict:
+    """Same step through the public API with host buffers: each step copies the
+    bf16 grads from pinned host memory and reads the updated bf16 parameters
+    back to pinned host memory, both inside the timed region."""
+    h = HYPER
+    host_grad = torch.empty(st.grad.numel(), dtype=st.grad.dtype, pin_memory=True)
+    host_grad.copy_(st.grad)
+    host_param = torch.empty(st.param.numel(), dtype=st.param.dtype, pin_memory=True)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t = 1000
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            t += 1
+            st.grad.copy_(host_grad, non_blocking=True)
+            st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, stream=stream)
+            host_param.copy_(st.param, non_blocking=True)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    n = sum(numels)
+    return {"value": n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(host_grad.numel() * host_grad.element_size()),
+            "d2h_bytes_per_step": int(host_param.numel() * host_param.element_size()),
+            "steps": steps}
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(total_params: int, chunk: int = 1 << 20, seed: int = 1):
+    """A bounded, seeded sample of the workload for the CPU oracle: group-aligned
+    chunks of the first layer's tensors (each group is independent, so any
+    group-aligned piece is a valid unit of the step)."""
+    import oracle as O
+    specs = [s for s in W.llama_tensor_list(MODEL) if s.name.startswith("layers.0.")]
+    pieces = []
+    left = total_params
+    gen = torch.Generator().manual_seed(seed)
+    for s in specs:
+        for off in range(0, s.numel, chunk):
+            n = min(chunk, s.numel - off)
+            if left <= 0:
+                break
+            n = min(n, left)
+            theta = torch.ones(n) if s.is_norm else torch.randn(n, generator=gen) * 0.02
+            g = (torch.randn(n, generator=gen) * 1e-3).to(torch.bfloat16)
+            gb = g.view(torch.int16).numpy().view(np.uint16)
+            pieces.append((O.TensorState.init(theta.numpy(), master_bits=MASTER_BITS), gb))
+            left -= n
+    return pieces
+
+
+def run_oracle_steps(pieces, steps: int, threads: int, t0: int = 1) -> float:
+    """Wall seconds for ``steps`` oracle steps over the sample (threads over pieces)."""
+    import oracle as O
+    h = HYPER
+
+    def one(p, t):
+        st, g = p
+        O.adamw_step(st, g, t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+
+    start = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for k in range(steps):
+            list(ex.map(lambda p: one(p, t0 + k), pieces))
+    return time.perf_counter() - start
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(sample_params: int, steps: int) -> dict:
+    cores = host_cores()
+    pieces = oracle_sample(sample_params)
+    n = sum(p[0].numel for p in pieces)
+    run_oracle_steps(pieces, 1, cores)  # first touch
+    sec = run_oracle_steps(pieces, steps, cores, t0=2)
+    return {"value": n * steps / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{n:,} params of layer 0 of the {MODEL.name} list in group-aligned 1M-element pieces, "
+                       f"{steps} steps, one thread per piece on {cores} host cores")}
+
+
+# ------------------------------------------------------------ main
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-sample", type=int, default=96 << 20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    numels = [s.numel for s in W.llama_tensor_list(MODEL)]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # each step: the oracle over a bounded 8M-parameter sample of the workload
+        cores = host_cores()
+        pieces = oracle_sample(8 << 20)
+        n = sum(p[0].numel for p in pieces)
+        run_oracle_steps(pieces, args.warmup, cores)
+        sec = run_oracle_steps(pieces, args.steps, cores, t0=args.warmup + 1)
+        v = n * args.steps / sec
+        line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "impl": "reference", "config": workload_config(numels),
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                 "sample": f"{n:,} params of layer 0 per step (group-aligned 1M pieces), "
+                                           f"one thread per piece on {cores} host cores"},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return
+
+    dist_on = ws > 1
+    if dist_on:
+        torch.distributed.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import quantized_state_optimizer_gb300 as fo
+    fo.lib()  # fail loudly if the CUDA library is missing
+
+    st, numels = build_state(device)
+    stream = torch.cuda.Stream(device=device)
+    with ClockSampler(local) as clk:
+        total_ms, per = time_steps(st, args.steps, args.warmup, stream, dist_on)
+    ms = total_ms / args.steps
+    if dist_on:
+        tt = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    n = sum(numels)
+    value = ws * n / (ms * 1e-3)
+    bytes_step = algorithmic_bytes(numels)
+    kernel_ms = statistics.mean(per)
+    peak, peak_kind = load_peak()
+    achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
+    try:
+        e2e = time_e2e(st, numels, args.e2e_steps, stream)
+    except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
+        e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
+    del st
+    torch.cuda.empty_cache()
+
+    if rank != 0:
+        if dist_on:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_sample, 3)
+    cfg = workload_config(numels)
+    cfg["bytes_per_step"] = bytes_step
+    cfg["bytes_per_param"] = bytes_step / n
+    cfg["hbm_gbs"] = achieved
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
+                     "kernel": "fo::adamw_step_kernel", "kernel_ms": kernel_ms,
+                     "bytes_per_launch": bytes_step, "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

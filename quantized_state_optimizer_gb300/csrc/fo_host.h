@@ -1,0 +1,30 @@
+// fo_host.h -- host-side helpers shared by the entry points of libfo.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fo.h"
+
+namespace fo {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int64_t n_groups(int64_t n) { return (n + 31) / 32; }
+
+// Remember the CUDA error of the calling thread's last failed launch.
+void record_cuda_error(cudaError_t e);
+
+// Turn the state after a launch into a status (FO_ERR_CUDA on a launch error).
+inline fo_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return FO_ERR_CUDA;
+  }
+  return FO_OK;
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace fo

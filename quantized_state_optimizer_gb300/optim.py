@@ -1,0 +1,187 @@
+"""FlashAdamW state containers and a ``torch.optim.Optimizer`` front end.
+
+``FlashAdamWState`` holds the optimizer state of a list of tensors in a few
+flat device slabs (one per buffer kind), each tensor at a 16-byte-aligned
+offset, and drives ``fo_adamw_step`` over the whole list in one call.
+
+``FlashAdamW`` is the drop-in optimizer for bf16 ``torch.nn.Parameter`` s,
+following ``FlashAdamWSim`` of the page "code/flashsim/flash_adamw_sim.py":
+lazily initialised state (quantized zeros, theta split on first use), the
+step count incremented before the update, parameters without a gradient
+skipped.  All arithmetic runs in libfo.so.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import FoTensor, fo_adamw_step, fo_split, n_groups
+
+_ALIGN_BYTES = 16
+
+
+def _align(n_elems: int, elem_bytes: int) -> int:
+    per = _ALIGN_BYTES // elem_bytes if elem_bytes < _ALIGN_BYTES else 1
+    return (n_elems + per - 1) // per * per
+
+
+class FlashAdamWState:
+    """Flat device buffers for the FlashAdamW state of ``numels`` tensors.
+
+    Per tensor: theta' (bf16), rho (int8 or int16), m codes (int8), m scales
+    (fp16), v codes (uint8), v scales (fp16), and optionally a grad buffer
+    (fp32 or bf16).  All start at zero: zero codes and scales are the
+    quantized zero state.
+    """
+
+    def __init__(self, numels, rho_bits: int = 8, grad_dtype=torch.bfloat16, device="cuda",
+                 with_grads: bool = True):
+        if rho_bits not in (8, 16):
+            raise ValueError("rho_bits must be 8 or 16")
+        self.numels = [int(n) for n in numels]
+        self.rho_bits = rho_bits
+        self.grad_dtype = grad_dtype
+        self.device = torch.device(device)
+        rho_dt = torch.int8 if rho_bits == 8 else torch.int16
+        self._off, self._goff = [], []
+        o = go = 0
+        for n in self.numels:
+            self._off.append(o)
+            self._goff.append(go)
+            o += _align(n, 1) if n else 0       # 16 elements: keeps every slab 16-byte aligned
+            go += _align(n_groups(n), 2) if n else 0
+        total, gtotal = max(o, 16), max(go, 8)
+        dev = self.device
+        self.param = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+        self.rho = torch.zeros(total, dtype=rho_dt, device=dev)
+        self.m_codes = torch.zeros(total, dtype=torch.int8, device=dev)
+        self.v_codes = torch.zeros(total, dtype=torch.uint8, device=dev)
+        self.m_scales = torch.zeros(gtotal, dtype=torch.float16, device=dev)
+        self.v_scales = torch.zeros(gtotal, dtype=torch.float16, device=dev)
+        self.grad = torch.zeros(total, dtype=grad_dtype, device=dev) if with_grads else None
+        self._fo_array = None
+
+    # ------------------------------------------------------------ views
+    def __len__(self) -> int:
+        return len(self.numels)
+
+    def _v(self, slab, i, n):
+        return slab[self._off[i]: self._off[i] + n]
+
+    def view(self, i: int) -> dict[str, torch.Tensor]:
+        n = self.numels[i]
+        g = n_groups(n)
+        go = self._goff[i]
+        d = {
+            "param": self._v(self.param, i, n), "rho": self._v(self.rho, i, n),
+            "m_codes": self._v(self.m_codes, i, n), "v_codes": self._v(self.v_codes, i, n),
+            "m_scales": self.m_scales[go: go + g], "v_scales": self.v_scales[go: go + g],
+        }
+        if self.grad is not None:
+            d["grad"] = self._v(self.grad, i, n)
+        return d
+
+    def grad_view(self, i: int) -> torch.Tensor:
+        return self._v(self.grad, i, self.numels[i])
+
+    def total_numel(self) -> int:
+        return sum(self.numels)
+
+    # ------------------------------------------------------------ set-up
+    def init_theta(self, i: int, theta: torch.Tensor, stream=None) -> None:
+        """Split an fp32 master weight into this tensor's theta' and rho."""
+        v = self.view(i)
+        fo_split(theta.reshape(-1).contiguous(), self.rho_bits, v["param"], v["rho"], stream)
+
+    def fo_tensors(self, grads=None):
+        """ctypes array of ``fo_tensor`` for all tensors (cached for the slab grads)."""
+        if grads is None and self._fo_array is not None:
+            return self._fo_array
+        arr = (FoTensor * max(len(self.numels), 1))()
+        for i, n in enumerate(self.numels):
+            v = self.view(i)
+            g = v["grad"] if grads is None else grads[i]
+            arr[i] = FoTensor(v["param"].data_ptr(), v["rho"].data_ptr(), g.data_ptr(),
+                              v["m_codes"].data_ptr(), v["m_scales"].data_ptr(),
+                              v["v_codes"].data_ptr(), v["v_scales"].data_ptr(), n)
+        if grads is None:
+            self._fo_array = arr
+        return arr
+
+    def step(self, step: int, lr: float, beta1: float, beta2: float, eps: float,
+             weight_decay: float, grads=None, stream=None) -> None:
+        """One fused FlashAdamW step over every tensor (one kernel launch)."""
+        arr = self.fo_tensors(grads)
+        gdt = self.grad_dtype if grads is None else grads[0].dtype
+        fo_adamw_step(arr, gdt, lr, beta1, beta2, eps, weight_decay, step, self.rho_bits, stream)
+
+    def state_dict(self) -> dict[str, torch.Tensor]:
+        """Host copies of every state slab (checkpoint)."""
+        return {k: getattr(self, k).cpu() for k in
+                ("param", "rho", "m_codes", "m_scales", "v_codes", "v_scales")}
+
+    def load_state_dict(self, sd: dict[str, torch.Tensor]) -> None:
+        for k, t in sd.items():
+            getattr(self, k).copy_(t)
+
+
+class FlashAdamW(torch.optim.Optimizer):
+    """AdamW with 8-bit group-quantized m and v and a bf16 + rho master weight.
+
+    Parameters must be bf16 CUDA tensors; their fp32 master weights live as
+    (theta' = the parameter itself, rho).  ``master_weight_bits`` = 24 (int8
+    rho) or 32 (int16 rho).  Gradients may be bf16 or fp32 (one dtype per
+    step call).  All parameters of all groups that have a gradient are updated
+    by one launch per param group.
+    """
+
+    def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0,
+                 master_weight_bits: int = 24):
+        if master_weight_bits not in (24, 32):
+            raise ValueError("master_weight_bits must be 24 or 32")
+        defaults = dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay)
+        super().__init__(params, defaults)
+        self.rho_bits = 8 if master_weight_bits == 24 else 16
+
+    def _init_state(self, p: torch.Tensor) -> dict:
+        if p.dtype != torch.bfloat16 or not p.is_cuda or not p.is_contiguous():
+            raise TypeError("FlashAdamW parameters must be contiguous bf16 CUDA tensors")
+        n = p.numel()
+        dev = p.device
+        st = self.state[p]
+        st["step"] = 0
+        st["rho"] = torch.zeros(n, dtype=torch.int8 if self.rho_bits == 8 else torch.int16, device=dev)
+        st["m_codes"] = torch.zeros(n, dtype=torch.int8, device=dev)
+        st["m_scales"] = torch.zeros(n_groups(n), dtype=torch.float16, device=dev)
+        st["v_codes"] = torch.zeros(n, dtype=torch.uint8, device=dev)
+        st["v_scales"] = torch.zeros(n_groups(n), dtype=torch.float16, device=dev)
+        # the parameter is already bf16: its master starts as the parameter itself (rho = 0)
+        return st
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        for group in self.param_groups:
+            beta1, beta2 = group["betas"]
+            by_key: dict[tuple[int, torch.dtype], list] = {}
+            for p in group["params"]:
+                if p.grad is None:
+                    continue
+                st = self.state[p]
+                if len(st) == 0:
+                    st = self._init_state(p)
+                st["step"] += 1
+                g = p.grad
+                if not g.is_contiguous():
+                    g = g.contiguous()
+                ft = FoTensor(p.data_ptr(), st["rho"].data_ptr(), g.data_ptr(), st["m_codes"].data_ptr(),
+                              st["m_scales"].data_ptr(), st["v_codes"].data_ptr(),
+                              st["v_scales"].data_ptr(), p.numel())
+                by_key.setdefault((st["step"], g.dtype), []).append((ft, g))
+            for (t, gdt), items in by_key.items():
+                fo_adamw_step([ft for ft, _ in items], gdt, group["lr"], beta1, beta2, group["eps"],
+                              group["weight_decay"], t, self.rho_bits)
+        return loss

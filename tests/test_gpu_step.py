@@ -1,0 +1,251 @@
+"""GPU parity of the fused multi-tensor FlashAdamW step against the CPU oracle.
+
+Both sides start from the same seeded fp32 master weights and zero states,
+split them independently, and then take the same seeded gradients step after
+step; theta', rho, codes and scales must stay identical bit for bit (which
+implies the looser targets: all codes within +/-1, theta within 1e-6).
+
+The full-size Llama lists are checked on sampled groups: every group evolves
+independently of all others, so the oracle carries a fixed sample of groups
+through all steps and is compared with the same groups of the GPU run.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import quantized_state_optimizer_gb300 as fo
+import workloads as W
+from quantized_state_optimizer_gb300.optim import FlashAdamW, FlashAdamWState
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+def _bits16(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def gpu_view_np(st: FlashAdamWState, i: int) -> dict:
+    v = st.view(i)
+    return {"param": _bits16(v["param"]), "rho": v["rho"].cpu().numpy(),
+            "m": v["m_codes"].cpu().numpy(), "m_scales": _bits16(v["m_scales"]),
+            "v": v["v_codes"].cpu().numpy(), "v_scales": _bits16(v["v_scales"])}
+
+
+def ref_np(r: O.TensorState) -> dict:
+    return {"param": r.param, "rho": r.rho, "m": r.m, "m_scales": r.m_scales, "v": r.v,
+            "v_scales": r.v_scales}
+
+
+def assert_same(got: dict, ref: dict, ctx):
+    for k in ("param", "rho", "m", "m_scales", "v", "v_scales"):
+        a, b = np.asarray(got[k]), np.asarray(ref[k])
+        assert a.shape == b.shape, (ctx, k, a.shape, b.shape)
+        if not np.array_equal(a, b):
+            bad = np.flatnonzero(a != b)
+            raise AssertionError(f"{ctx}: {k} differs at {bad.size} of {a.size} (first {bad[:5]})")
+
+
+def tolerance_report(got: dict, ref: dict, master_bits: int) -> dict:
+    """The looser parity targets: code agreement, codes within +/-1, theta rel. error."""
+    out = {}
+    for k in ("m", "v"):
+        d = np.abs(got[k].astype(int) - ref[k].astype(int))
+        out[k + "_identical"] = float(np.mean(d == 0))
+        out[k + "_within1"] = float(np.mean(d <= 1))
+    tg = O.reconstruct(got["param"], got["rho"], master_bits).astype(np.float64)
+    tr = O.reconstruct(ref["param"], ref["rho"], master_bits).astype(np.float64)
+    nz = tr != 0
+    out["theta_max_rel_err"] = float(np.max(np.abs(tg[nz] - tr[nz]) / np.abs(tr[nz]))) if nz.any() else 0.0
+    return out
+
+
+def _grad(i: int, t: int, n: int, dtype) -> torch.Tensor:
+    g = torch.Generator().manual_seed(W.grad_seed(99, i, t))
+    x = torch.randn(n, generator=g) * 1e-3
+    return x if dtype == torch.float32 else x.to(torch.bfloat16)
+
+
+def run_small(numels, rho_bits, grad_dtype, hyper: W.Hyper, steps: int, theta_fn=None):
+    mb = 24 if rho_bits == 8 else 32
+    st = FlashAdamWState(numels, rho_bits=rho_bits, grad_dtype=grad_dtype, device=DEV)
+    refs = []
+    for i, n in enumerate(numels):
+        theta = theta_fn(i, n) if theta_fn else torch.randn(n, generator=torch.Generator().manual_seed(i)) * 0.02
+        if n:
+            st.init_theta(i, theta.to(DEV))
+        refs.append(O.TensorState.init(theta.numpy(), master_bits=mb))
+    for t in range(1, steps + 1):
+        for i, n in enumerate(numels):
+            if n == 0:
+                continue
+            g = _grad(i, t, n, grad_dtype)
+            st.grad_view(i).copy_(g.to(DEV))
+            gn = g.numpy() if grad_dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16)
+            O.adamw_step(refs[i], gn, t, hyper.lr, hyper.beta1, hyper.beta2, hyper.eps, hyper.weight_decay)
+        st.step(t, hyper.lr, hyper.beta1, hyper.beta2, hyper.eps, hyper.weight_decay)
+        torch.cuda.synchronize()
+        for i, n in enumerate(numels):
+            if n:
+                assert_same(gpu_view_np(st, i), ref_np(refs[i]), (numels[i], rho_bits, grad_dtype, t))
+    return st, refs
+
+
+def test_single_tensor_65553_fp32_grads_10_steps():
+    """One flat tensor of 2^16+17 parameters, fp32 grads, 24-bit master, 10 steps."""
+    n = W.SINGLE_TENSOR_NUMEL
+    h = W.SINGLE_TENSOR_HYPER
+    st = FlashAdamWState([n], rho_bits=8, grad_dtype=torch.float32, device=DEV)
+    theta = W.single_tensor_theta(n)
+    st.init_theta(0, theta.to(DEV))
+    ref = O.TensorState.init(theta.numpy(), master_bits=24)
+    for t in range(1, h.steps + 1):
+        g = W.single_tensor_grad(t, n)
+        st.grad_view(0).copy_(g.to(DEV))
+        O.adamw_step(ref, g.numpy(), t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        torch.cuda.synchronize()
+        got = gpu_view_np(st, 0)
+        assert_same(got, ref_np(ref), ("single", t))
+    rep = tolerance_report(got, ref_np(ref), 24)
+    assert rep["m_identical"] == 1.0 and rep["v_identical"] == 1.0 and rep["theta_max_rel_err"] == 0.0
+
+
+@pytest.mark.parametrize("rho_bits", [8, 16])
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_mixed_ragged_list(rho_bits, grad_dtype, wd):
+    numels = [1, 31, 33, 4096, 4097, 0, 16, 100003, 65536, 8191]
+    h = W.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=wd, steps=3)
+    run_small(numels, rho_bits, grad_dtype, h, 3)
+
+
+def test_more_tensors_than_one_launch():
+    rng = np.random.default_rng(0)
+    count = fo.fo_max_tensors_per_launch() + 57
+    numels = [int(x) for x in rng.integers(1, 300, count)]
+    run_small(numels, 8, torch.bfloat16, W.LLAMA3_8B_HYPER, 2)
+
+
+def test_edge_values_in_state():
+    """Heavy-tailed master weights (huge, tiny, subnormal, zero) and large gradients."""
+    def theta_fn(i, n):
+        g = torch.Generator().manual_seed(100 + i)
+        x = torch.randn(n, generator=g) * torch.exp(torch.randn(n, generator=g) * 8)
+        x[::7] = 0.0
+        x[3::11] = 1e-39
+        return x.float()
+    run_small([4096 + 5, 1000], 8, torch.float32, W.SINGLE_TENSOR_HYPER, 3, theta_fn)
+    run_small([4096 + 5, 1000], 16, torch.float32, W.SINGLE_TENSOR_HYPER, 3, theta_fn)
+
+
+def test_checkpoint_resume_is_bit_identical():
+    numels = [5000, 4096, 77]
+    h = W.TINYLLAMA_HYPER
+
+    def make():
+        st = FlashAdamWState(numels, rho_bits=16, grad_dtype=torch.bfloat16, device=DEV)
+        for i, n in enumerate(numels):
+            st.init_theta(i, (torch.randn(n, generator=torch.Generator().manual_seed(i)) * 0.02).to(DEV))
+        return st
+
+    def run(st, t0, t1):
+        for t in range(t0, t1 + 1):
+            for i, n in enumerate(numels):
+                st.grad_view(i).copy_(_grad(i, t, n, torch.bfloat16).to(DEV))
+            st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+
+    a = make()
+    run(a, 1, 10)
+    b = make()
+    run(b, 1, 5)
+    sd = b.state_dict()
+    c = make()
+    c.load_state_dict(sd)
+    run(c, 6, 10)
+    torch.cuda.synchronize()
+    for k in ("param", "rho", "m_codes", "m_scales", "v_codes", "v_scales"):
+        assert torch.equal(getattr(a, k).view(torch.uint8) if getattr(a, k).dtype != torch.uint8 else getattr(a, k),
+                           getattr(c, k).view(torch.uint8) if getattr(c, k).dtype != torch.uint8 else getattr(c, k)), k
+
+
+def test_torch_optimizer_front_end_matches_oracle():
+    torch.manual_seed(0)
+    shapes = [(64, 33), (4097,), (7,)]
+    params = [torch.nn.Parameter((torch.randn(s) * 0.02).to(torch.bfloat16).to(DEV)) for s in shapes]
+    refs = [O.TensorState.init(p.detach().float().cpu().numpy().reshape(-1), master_bits=24) for p in params]
+    opt = FlashAdamW(params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01)
+    for t in range(1, 4):
+        for i, p in enumerate(params):
+            g = _grad(i, t, p.numel(), torch.bfloat16)
+            p.grad = g.reshape(p.shape).to(DEV)
+            O.adamw_step(refs[i], g.view(torch.int16).numpy().view(np.uint16), t, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+        opt.step()
+    torch.cuda.synchronize()
+    for p, r in zip(params, refs):
+        s = opt.state[p]
+        got = {"param": _bits16(p.detach().reshape(-1)), "rho": s["rho"].cpu().numpy(),
+               "m": s["m_codes"].cpu().numpy(), "m_scales": _bits16(s["m_scales"]),
+               "v": s["v_codes"].cpu().numpy(), "v_scales": _bits16(s["v_scales"])}
+        assert_same(got, ref_np(r), "FlashAdamW")
+
+
+def test_argument_errors_through_binding():
+    st = FlashAdamWState([100], rho_bits=8, device=DEV)
+    with pytest.raises(fo.FoError, match="INVALID_ARG"):
+        st.step(0, 1e-3, 0.9, 0.999, 1e-8, 0.0)
+    with pytest.raises(fo.FoError, match="INVALID_ARG"):
+        st.step(1, 1e-3, 1.0, 0.999, 1e-8, 0.0)
+    arr = st.fo_tensors()
+    bad = (fo.FoTensor * 2)(arr[0], arr[0])  # the same buffers twice
+    with pytest.raises(fo.FoError, match="ALIAS"):
+        fo.fo_adamw_step(bad, torch.bfloat16, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8)
+
+
+# ------------------------------------------------------------ full size
+def run_full_size(model: W.ModelShape, hyper: W.Hyper, master_bits: int, groups_per_tensor: int = 24,
+                  check_steps=(1, 10, 20)):
+    rho_bits = 8 if master_bits == 24 else 16
+    wid = W.WORKLOAD_IDS[model.name]
+    specs = W.llama_tensor_list(model)
+    numels = [s.numel for s in specs]
+    st = FlashAdamWState(numels, rho_bits=rho_bits, grad_dtype=torch.bfloat16, device=DEV)
+    idx, gidx, refs = [], [], []
+    for i, s in enumerate(specs):
+        gi = W.sample_group_indices(s.numel, groups_per_tensor, seed=1000 + i)
+        e = (gi.view(-1, 1) * 32 + torch.arange(32).view(1, -1)).reshape(-1)
+        e = e[e < s.numel]
+        theta = W.init_theta(s, wid, i, DEV)
+        st.init_theta(i, theta)
+        refs.append(O.TensorState.init(theta[e.to(DEV)].cpu().numpy(), master_bits=master_bits))
+        del theta
+        idx.append(e.to(DEV))
+        gidx.append(gi.to(DEV))
+    for t in range(1, hyper.steps + 1):
+        for i, s in enumerate(specs):
+            gv = st.grad_view(i)
+            W.make_grad(s.numel, wid, i, t, DEV, out=gv)
+            gs = gv[idx[i]].cpu().view(torch.int16).numpy().view(np.uint16)
+            O.adamw_step(refs[i], gs, t, hyper.lr, hyper.beta1, hyper.beta2, hyper.eps, hyper.weight_decay)
+        st.step(t, hyper.lr, hyper.beta1, hyper.beta2, hyper.eps, hyper.weight_decay)
+        if t in check_steps:
+            torch.cuda.synchronize()
+            for i in range(len(specs)):
+                v = st.view(i)
+                got = {"param": _bits16(v["param"][idx[i]]), "rho": v["rho"][idx[i]].cpu().numpy(),
+                       "m": v["m_codes"][idx[i]].cpu().numpy(), "m_scales": _bits16(v["m_scales"][gidx[i]]),
+                       "v": v["v_codes"][idx[i]].cpu().numpy(), "v_scales": _bits16(v["v_scales"][gidx[i]])}
+                assert_same(got, ref_np(refs[i]), (model.name, specs[i].name, t))
+    return st
+
+
+def test_llama_1b_list_int16_rho_20_steps_sampled():
+    st = run_full_size(W.TINYLLAMA_1B, W.TINYLLAMA_HYPER, W.TINYLLAMA_MASTER_BITS)
+    assert st.total_numel() == 1_100_048_384 and len(st) == 201
+
+
+def test_llama3_8b_list_int8_rho_20_steps_sampled():
+    st = run_full_size(W.LLAMA3_8B, W.LLAMA3_8B_HYPER, W.LLAMA3_8B_MASTER_BITS, groups_per_tensor=16)
+    assert st.total_numel() == 8_030_261_248 and len(st) == 291
