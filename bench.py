@@ -129,15 +129,27 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ GPU arm
-def build_state(device):
-    from quantized_state_optimizer_gb300.optim import FlashAdamWState
+def bench_specs(layers: int | None):
+    """The full tensor list, or (for profiling captures that must stay small) only
+    the tensors of the first ``layers`` decoder layers."""
     specs = W.llama_tensor_list(MODEL)
+    if layers is None:
+        return specs
+    keep = tuple(f"layers.{i}." for i in range(layers))
+    return [s for s in specs if s.name.startswith(keep)]
+
+
+def build_state(device, layers: int | None = None):
+    from quantized_state_optimizer_gb300.optim import FlashAdamWState
+    all_specs = W.llama_tensor_list(MODEL)
+    specs = bench_specs(layers)
     numels = [s.numel for s in specs]
     wid = W.WORKLOAD_IDS[MODEL.name]
     st = FlashAdamWState(numels, rho_bits=RHO_BITS, grad_dtype=torch.bfloat16, device=device)
     for i, s in enumerate(specs):
-        st.init_theta(i, W.init_theta(s, wid, i, device))
-        W.make_grad(s.numel, wid, i, 1, device, out=st.grad_view(i))
+        k = all_specs.index(s)  # seeds follow the tensor's index in the full list
+        st.init_theta(i, W.init_theta(s, wid, k, device))
+        W.make_grad(s.numel, wid, k, 1, device, out=st.grad_view(i))
     torch.cuda.synchronize()
     return st, numels
 
@@ -275,6 +287,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-sample", type=int, default=96 << 20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling only: restrict to the first N decoder layers' tensors")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     numels = [s.numel for s in W.llama_tensor_list(MODEL)]
@@ -309,7 +323,7 @@ def main():
     import quantized_state_optimizer_gb300 as fo
     fo.lib()  # fail loudly if the CUDA library is missing
 
-    st, numels = build_state(device)
+    st, numels = build_state(device, args.layers)
     stream = torch.cuda.Stream(device=device)
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(st, args.steps, args.warmup, stream, dist_on)
@@ -325,7 +339,7 @@ def main():
     peak, peak_kind = load_peak()
     achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
     try:
-        e2e = time_e2e(st, numels, args.e2e_steps, stream)
+        e2e = time_e2e(st, numels, args.e2e_steps, stream) if args.e2e_steps > 0 else None
     except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
         e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
     del st
@@ -339,6 +353,8 @@ def main():
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_sample, 3)
     cfg = workload_config(numels)
+    if args.layers is not None:
+        cfg["workload"] = f"PROFILING SUBSET (first {args.layers} layers) of " + cfg["workload"]
     cfg["bytes_per_step"] = bytes_step
     cfg["bytes_per_param"] = bytes_step / n
     cfg["hbm_gbs"] = achieved
