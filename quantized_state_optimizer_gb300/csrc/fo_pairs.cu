@@ -53,10 +53,28 @@ __global__ void __launch_bounds__(kThreads)
   const float safe = guarded_divisor(s16);
 
   V16B out;
+  if constexpr (kSigned == kSoftsign) {
+    // momentum (softsign) and both unsigned specs (r c2 = 255 r/s whether or
+    // not r is a square root): certified approximate codes, exact where uncertain
+    const float rs = __fdiv_rn(1.0f, safe);
+    const float c1 = __fmul_rn(254.0f, rs);
+    const float c2 = __fdiv_rn(255.0f, safe);
+    uint32_t near = 0;
 #pragma unroll
-  for (int j = 0; j < kPerThread; ++j) {
-    const int q = encode_code<kSigned, kSoftsign>(r[j], safe);
-    out.u8[j] = static_cast<uint8_t>(q);
+    for (int j = 0; j < kPerThread; ++j) {
+      bool nj;
+      const float t = kSigned ? momentum_t_approx(r[j], rs, c1) : variance_t_approx_from_root(r[j], c2);
+      out.u8[j] = round_code_certified(t, nj);
+      if (nj) near |= 1u << j;
+    }
+    if (near) {
+#pragma unroll
+      for (int j = 0; j < kPerThread; ++j)
+        if (near & (1u << j)) out.u8[j] = static_cast<uint8_t>(encode_code<kSigned, kSoftsign>(r[j], safe));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) out.u8[j] = static_cast<uint8_t>(encode_code<kSigned, kSoftsign>(r[j], safe));
   }
   uint8_t* c = static_cast<uint8_t*>(codes);
   if (e0 + kPerThread <= n) {

@@ -65,6 +65,41 @@ def test_quantize_ragged_sizes(n):
         assert same_f32(d, O.dequantize(rc, rs, spec))
 
 
+def _boundary_inputs(spec: str) -> np.ndarray:
+    """Groups whose first element fixes the scale at exactly 1.0 and whose other
+    elements sit on, and a few ulps around, the inputs where the code argument
+    is exactly k + 1/2 (round-half-even territory): every one of them must
+    take the exact path and still agree with the oracle."""
+    out = []
+    ks = np.arange(0, 127) if spec == "momentum" else np.arange(0, 255)
+    for k in ks:
+        if spec == "momentum":
+            z = (k + 0.5) / 127.0
+            x0 = z / (2.0 - z)            # inverse softsign at scale 1
+        else:
+            x0 = ((k + 0.5) / 255.0) ** 2  # inverse of 255 sqrt(v)
+        x0 = np.float32(x0)
+        nb = [np.float32(np.nextafter(x0, np.float32(np.inf * d))) for d in (1, -1)]
+        cand = [x0, nb[0], nb[1], np.float32(np.nextafter(nb[0], np.float32(np.inf))),
+                np.float32(np.nextafter(nb[1], np.float32(-np.inf)))]
+        g = np.zeros(32, np.float32)
+        g[0] = 1.0
+        g[1:1 + len(cand)] = cand
+        if spec == "momentum":
+            g[8:8 + len(cand)] = [-c for c in cand]
+        out.append(g)
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("spec", ["momentum", "variance"])
+def test_quantize_half_code_boundaries(spec):
+    x = _boundary_inputs(spec)
+    c, s, d = gpu_quantize(x, spec)
+    rc, rs = O.quantize(x, spec)
+    assert np.array_equal(s, rs)
+    assert np.array_equal(c, rc), np.flatnonzero(c != rc)[:10]
+
+
 def test_quantize_does_not_write_past_n():
     n = 4097
     x = torch.randn(n, device=DEV)

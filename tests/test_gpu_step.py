@@ -141,6 +141,34 @@ def test_edge_values_in_state():
     run_small([4096 + 5, 1000], 16, torch.float32, W.SINGLE_TENSOR_HYPER, 3, theta_fn)
 
 
+@pytest.mark.parametrize("rho_bits", [8, 16])
+def test_volume_heavy_tailed_parity(rho_bits):
+    """Millions of elements with gradients and weights spread over many orders
+    of magnitude, so that uncertain codes and uncertain 24-bit masters (the
+    exact fallbacks of the kernel) occur thousands of times per step."""
+    numels = [(1 << 22) + 7, 3 * (1 << 20)]
+    mb = 24 if rho_bits == 8 else 32
+    h = W.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.05, steps=4)
+    st = FlashAdamWState(numels, rho_bits=rho_bits, grad_dtype=torch.bfloat16, device=DEV)
+    refs = []
+    for i, n in enumerate(numels):
+        gen = torch.Generator().manual_seed(500 + i)
+        theta = torch.randn(n, generator=gen) * torch.exp(torch.randn(n, generator=gen) * 2) * 0.02
+        st.init_theta(i, theta.to(DEV))
+        refs.append(O.TensorState.init(theta.numpy(), master_bits=mb))
+    for t in range(1, h.steps + 1):
+        for i, n in enumerate(numels):
+            gen = torch.Generator().manual_seed(W.grad_seed(77, i, t))
+            g = (torch.randn(n, generator=gen) * torch.exp(torch.randn(n, generator=gen) * 3) * 1e-3).to(torch.bfloat16)
+            st.grad_view(i).copy_(g.to(DEV))
+            O.adamw_step(refs[i], g.view(torch.int16).numpy().view(np.uint16), t, h.lr, h.beta1, h.beta2,
+                         h.eps, h.weight_decay)
+        st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        torch.cuda.synchronize()
+        for i in range(len(numels)):
+            assert_same(gpu_view_np(st, i), ref_np(refs[i]), ("volume", rho_bits, i, t))
+
+
 def test_checkpoint_resume_is_bit_identical():
     numels = [5000, 4096, 77]
     h = W.TINYLLAMA_HYPER
