@@ -1,0 +1,29 @@
+"""The step kernel certifies results computed with rcp.approx / sqrt.approx
+against error bounds that assume at most 2 units in the last place for each.
+This measures the worst case of both over every positive normal fp32 input on
+the device in use and checks it against that assumption."""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from quantized_state_optimizer_gb300 import build as B
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ASSUMED_MAX_ULP = 2
+
+
+def test_hardware_approximation_error_within_assumed_bound(tmp_path):
+    so = str(tmp_path / "approx_probe.so")
+    subprocess.run([B.nvcc(), *B.ARCH, "-O3", "-Xcompiler", "-fPIC", "-shared", "-o", so,
+                    os.path.join(HERE, "native", "approx_probe.cu")], check=True)
+    lib = ctypes.CDLL(so)
+    out = (ctypes.c_uint * 2)()
+    assert lib.approx_probe(out) == 0
+    rcp_ulp, sqrt_ulp = out[0], out[1]
+    print(f"rcp.approx.ftz max {rcp_ulp} ulp, sqrt.approx.ftz max {sqrt_ulp} ulp")
+    assert rcp_ulp <= ASSUMED_MAX_ULP and sqrt_ulp <= ASSUMED_MAX_ULP
