@@ -150,6 +150,15 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
 /* Largest tensor list fo_adamw_step handles in a single kernel launch. */
 int fo_max_tensors_per_launch(void);
 
+/* Device-side status of fo_adamw_step on the current device, then cleared.
+ * The step kernel never waits without a limit: if a bulk load it waits for
+ * has not arrived after a bounded number of polls, that block stops and sets
+ * bit 0 (FO_DEVICE_WAIT_TIMEOUT); its tiles are then left unprocessed.  The
+ * call synchronizes with the device (it copies one word), so use it for
+ * diagnostics, not on the hot path.  *status = 0 means no such event. */
+#define FO_DEVICE_WAIT_TIMEOUT 1u
+fo_status fo_device_status(uint32_t* status);
+
 #ifdef __cplusplus
 }
 #endif

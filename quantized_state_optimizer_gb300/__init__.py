@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "FoError", "SPECS", "fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct",
-    "fo_adamw_step", "fo_max_tensors_per_launch", "FoTensor", "lib", "lib_path",
+    "fo_adamw_step", "fo_max_tensors_per_launch", "fo_device_status", "FoTensor", "lib", "lib_path",
 ]
 
 SPECS = {"momentum": 0, "variance": 1, "momentum_linear": 2, "variance_linear": 3}
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.fo_split.argtypes = [p, i64, i32, p, p, p]
         L.fo_reconstruct.argtypes = [p, p, i64, i32, p, p]
         L.fo_adamw_step.argtypes = [ctypes.POINTER(FoTensor), i32, i32, d, d, d, d, d, i64, i32, p]
+        L.fo_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        L.fo_device_status.restype = i32
         L.fo_max_tensors_per_launch.argtypes = []
         L.fo_max_tensors_per_launch.restype = i32
         for f in ("fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct", "fo_adamw_step"):
@@ -166,6 +168,14 @@ def fo_reconstruct(theta_bf16: torch.Tensor, rho: torch.Tensor, rho_bits: int, t
 # ------------------------------------------------------------------ step
 def fo_max_tensors_per_launch() -> int:
     return lib().fo_max_tensors_per_launch()
+
+
+def fo_device_status() -> int:
+    """Device status word of the step kernel (0 = no bounded wait ran out); clears it.
+    Synchronizes with the device."""
+    out = ctypes.c_uint32(0)
+    _check("fo_device_status", lib().fo_device_status(ctypes.byref(out)))
+    return out.value
 
 
 def make_fo_tensor(param: torch.Tensor, rho: torch.Tensor, grad: torch.Tensor, m_codes: torch.Tensor,

@@ -220,6 +220,13 @@ def test_torch_optimizer_front_end_matches_oracle():
         assert_same(got, ref_np(r), "FlashAdamW")
 
 
+def test_device_status_clear_after_steps():
+    fo.fo_device_status()  # clear anything left by earlier tests
+    run_small([20000, 7680 * 3, 7680 + 5], 8, torch.bfloat16, W.LLAMA3_8B_HYPER, 2)
+    torch.cuda.synchronize()
+    assert fo.fo_device_status() == 0
+
+
 def test_argument_errors_through_binding():
     st = FlashAdamWState([100], rho_bits=8, device=DEV)
     with pytest.raises(fo.FoError, match="INVALID_ARG"):
