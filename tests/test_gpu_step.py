@@ -220,6 +220,14 @@ def test_torch_optimizer_front_end_matches_oracle():
         assert_same(got, ref_np(r), "FlashAdamW")
 
 
+def test_zero_initialized_weights_overflow_the_redo_queue():
+    """theta = 0 makes the new theta equal to -delta, whose 24-bit master is
+    uncertain for about one element in eight -- more per tile than the redo
+    queue holds, so the in-thread exact path runs too."""
+    numels = [7680 * 4, 7680 * 2 + 33]
+    run_small(numels, 8, torch.bfloat16, W.LLAMA3_8B_HYPER, 3, theta_fn=lambda i, n: torch.zeros(n))
+
+
 def test_device_status_clear_after_steps():
     fo.fo_device_status()  # clear anything left by earlier tests
     run_small([20000, 7680 * 3, 7680 + 5], 8, torch.bfloat16, W.LLAMA3_8B_HYPER, 2)
