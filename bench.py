@@ -61,6 +61,33 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
     return total
 
 
+# DRAM bytes (read + write) per parameter of the step kernel, from one ncu
+# capture on layer 0 of the list (profiles/adamw_step_llama3_8b_layer0_ncu.md):
+# 1.554722 GB read + 1.062141 GB written for 218,112,000 parameters.  Traffic
+# grows with the parameters processed, so a full launch is that figure times
+# the list's size.  It stands only for the kernel sources it was taken on.
+TRAFFIC_CAPTURE = {
+    "bytes_per_param": (1.554722e9 + 1.062141e9) / 218112000,
+    "sha256": {
+        "quantized_state_optimizer_gb300/csrc/fo_step.cu": "6a467c46e1e2469d206ef54925fbfb062aa9df30eb427487979898a028aeff09",
+        "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
+    },
+}
+
+
+def captured_traffic(n_params: int) -> float | None:
+    """Per-launch DRAM traffic scaled from the capture, or None once the kernel changed."""
+    import hashlib
+    for rel, digest in TRAFFIC_CAPTURE["sha256"].items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as fh:
+                if hashlib.sha256(fh.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return TRAFFIC_CAPTURE["bytes_per_param"] * n_params
+
+
 def load_peak() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -365,7 +392,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
                      "kernel": "fo::adamw_step_kernel", "kernel_ms": kernel_ms,
-                     "bytes_per_launch": bytes_step, "traffic": None},
+                     "bytes_per_launch": bytes_step,
+                     "traffic": captured_traffic(n) if args.layers is None else None},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
