@@ -211,32 +211,33 @@ def time_steps(st, steps: int, warmup: int, stream, dist_on: bool) -> tuple[floa
 
 
 def time_e2e(st, numels, steps: int, stream) -> dict:
-    """Same step through the public API with host buffers: each step copies the
-    bf16 grads from pinned host memory and reads the updated bf16 parameters
-    back to pinned host memory, both inside the timed region."""
+    """Same step through the public API with host buffers: each step uploads the
+    bf16 grads from pinned host memory and downloads the updated bf16
+    parameters into pinned host memory (``FlashAdamWState.step_from_host``,
+    which overlaps both copies with the step chunk by chunk), all inside the
+    timed region."""
     h = HYPER
     host_grad = torch.empty(st.grad.numel(), dtype=st.grad.dtype, pin_memory=True)
     host_grad.copy_(st.grad)
     host_param = torch.empty(st.param.numel(), dtype=st.param.dtype, pin_memory=True)
     torch.cuda.synchronize()
+    t = 1000
+    st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param, stream=stream)
+    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t = 1000
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(steps):
-            t += 1
-            st.grad.copy_(host_grad, non_blocking=True)
-            st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, stream=stream)
-            host_param.copy_(st.param, non_blocking=True)
-        t1.record(stream)
+    t0.record(stream)
+    for _ in range(steps):
+        t += 1
+        st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param, stream=stream)
+    t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
     n = sum(numels)
     return {"value": n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(host_grad.numel() * host_grad.element_size()),
             "d2h_bytes_per_step": int(host_param.numel() * host_param.element_size()),
-            "steps": steps}
+            "steps": steps, "api": "FlashAdamWState.step_from_host (8 chunks, copies overlapped)"}
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -115,6 +115,65 @@ class FlashAdamWState:
         gdt = self.grad_dtype if grads is None else grads[0].dtype
         fo_adamw_step(arr, gdt, lr, beta1, beta2, eps, weight_decay, step, self.rho_bits, stream)
 
+    def _chunks(self, n_chunks: int):
+        """Contiguous groups of tensors with about equal element counts:
+        (first tensor, end tensor, slab start, slab end) each."""
+        key = ("chunks", n_chunks)
+        if getattr(self, "_chunk_key", None) == key:
+            return self._chunk_list
+        total = max(self.total_numel(), 1)
+        out, first, acc = [], 0, 0
+        for i, n in enumerate(self.numels):
+            acc += n
+            if acc * n_chunks >= total * (len(out) + 1) or i == len(self.numels) - 1:
+                end = i + 1
+                lo = self._off[first]
+                hi = self._off[end] if end < len(self.numels) else self.param.numel()
+                arr = (FoTensor * (end - first))(*[self.fo_tensors()[j] for j in range(first, end)])
+                out.append((first, end, lo, hi, arr))
+                first = end
+        self._chunk_key, self._chunk_list = key, out
+        return out
+
+    def step_from_host(self, step: int, lr: float, beta1: float, beta2: float, eps: float,
+                       weight_decay: float, host_grad: torch.Tensor, host_param: torch.Tensor,
+                       n_chunks: int = 8, stream=None) -> None:
+        """One step fed from host memory: upload the gradients from ``host_grad``
+        (pinned, laid out like the grad slab), step, and download the new theta'
+        into ``host_param`` (pinned, laid out like the param slab).
+
+        The list is cut into ``n_chunks`` groups of tensors.  Chunk c's upload,
+        step launch and download run on three streams chained by events, so the
+        copies of one chunk overlap the step of another and the two copy
+        directions overlap each other.  Everything is ordered after the work
+        already on ``stream`` (default: the current stream), and ``stream``
+        waits for the last download, so a later step or a synchronize on it
+        sees the finished parameters."""
+        if self.grad is None:
+            raise RuntimeError("step_from_host needs the grad slab (with_grads=True)")
+        if host_grad.numel() != self.grad.numel() or host_param.numel() != self.param.numel():
+            raise ValueError("host buffers must match the grad and param slabs")
+        compute = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if not hasattr(self, "_copy_streams"):
+            self._copy_streams = (torch.cuda.Stream(self.device), torch.cuda.Stream(self.device))
+        up, down = self._copy_streams
+        up.wait_stream(compute)  # the previous step no longer reads the grad slab
+        down.wait_stream(compute)
+        for first, end, lo, hi, arr in self._chunks(n_chunks):
+            with torch.cuda.stream(up):
+                self.grad[lo:hi].copy_(host_grad[lo:hi], non_blocking=True)
+                uploaded = torch.cuda.Event()
+                uploaded.record(up)
+            compute.wait_event(uploaded)
+            fo_adamw_step(arr, self.grad_dtype, lr, beta1, beta2, eps, weight_decay, step, self.rho_bits,
+                          compute)
+            stepped = torch.cuda.Event()
+            stepped.record(compute)
+            down.wait_event(stepped)
+            with torch.cuda.stream(down):
+                host_param[lo:hi].copy_(self.param[lo:hi], non_blocking=True)
+        compute.wait_stream(down)
+
     def state_dict(self) -> dict[str, torch.Tensor]:
         """Host copies of every state slab (checkpoint)."""
         return {k: getattr(self, k).cpu() for k in

@@ -199,6 +199,39 @@ def test_checkpoint_resume_is_bit_identical():
                            getattr(c, k).view(torch.uint8) if getattr(c, k).dtype != torch.uint8 else getattr(c, k)), k
 
 
+@pytest.mark.parametrize("n_chunks", [1, 3, 8])
+def test_step_from_host_matches_device_step(n_chunks):
+    """The host-fed step (chunked uploads, launches and downloads on three
+    streams) leaves the same state as device steps on the same gradients, and
+    the host copy of theta' equals the device one after every step."""
+    numels = [70000, 33, 4096 * 3, 0, 12345, 9000, 1]
+    h = W.LLAMA3_8B_HYPER
+
+    def make():
+        st = FlashAdamWState(numels, rho_bits=8, grad_dtype=torch.bfloat16, device=DEV)
+        for i, n in enumerate(numels):
+            if n:
+                st.init_theta(i, (torch.randn(n, generator=torch.Generator().manual_seed(i)) * 0.02).to(DEV))
+        return st
+
+    a, b = make(), make()
+    host_grad = torch.empty(b.grad.numel(), dtype=b.grad.dtype, pin_memory=True)
+    host_param = torch.empty(b.param.numel(), dtype=b.param.dtype, pin_memory=True)
+    for t in range(1, 5):
+        for i, n in enumerate(numels):
+            if n:
+                a.grad_view(i).copy_(_grad(i, t, n, torch.bfloat16).to(DEV))
+        host_grad.copy_(a.grad.cpu())
+        a.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        b.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param,
+                         n_chunks=n_chunks)
+        torch.cuda.synchronize()
+        for k in ("param", "rho", "m_codes", "m_scales", "v_codes", "v_scales"):
+            x, y = getattr(a, k), getattr(b, k)
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), (k, t)
+        assert torch.equal(host_param.view(torch.int16), b.param.cpu().view(torch.int16)), t
+
+
 def test_torch_optimizer_front_end_matches_oracle():
     torch.manual_seed(0)
     shapes = [(64, 33), (4097,), (7,)]
