@@ -49,7 +49,8 @@ typedef enum {
   FO_ERR_INVALID_ARG = 1, /* null pointer with n > 0, n < 0, bad enum, bad hyper-parameter */
   FO_ERR_MISALIGNED = 2,  /* a pointer not on a 16-byte boundary */
   FO_ERR_CUDA = 3,        /* the CUDA runtime refused a launch; see fo_last_cuda_error() */
-  FO_ERR_ALIAS = 4        /* fo_adamw_step: a written buffer overlaps another buffer */
+  FO_ERR_ALIAS = 4,       /* fo_adamw_step: a written buffer overlaps another buffer */
+  FO_ERR_TOO_LARGE = 5    /* fo_adamw_step_static: more tensors than FO_STATIC_MAX_TENSORS */
 } fo_status;
 
 /* Quantization spec of a state tensor.  MOMENTUM: signed int8, softsign
@@ -158,6 +159,33 @@ int fo_max_tensors_per_launch(void);
  * diagnostics, not on the hot path.  *status = 0 means no such event. */
 #define FO_DEVICE_WAIT_TIMEOUT 1u
 fo_status fo_device_status(uint32_t* status);
+
+/* ---- allocation-free step -------------------------------------------------
+ * No counterpart on the pages: an interface of this library.  Same arguments,
+ * results and errors as fo_adamw_step, for a list of at most
+ * FO_STATIC_MAX_TENSORS tensors, always in a single launch, and without
+ * allocating anything: the tensor list travels in a fixed device array of the
+ * library (about 74 KB per device) instead of the kernel's parameter block,
+ * and the host side works in fixed static storage.  It serves callers that
+ * must not allocate when they step, e.g. a loop that reserves all device
+ * memory for its own pools up front, or code that runs while an allocator's
+ * lock is held.
+ *   - n_tensors > FO_STATIC_MAX_TENSORS returns FO_ERR_TOO_LARGE before any
+ *     other check or CUDA call.
+ *   - Set-up: the first call on each device looks up the device address of
+ *     the array (cudaGetSymbolAddress; FO_ERR_CUDA if that fails).  Make the
+ *     first call on a device before any stream capture.
+ *   - Each call copies the list into the array (cudaMemcpyAsync on `stream`,
+ *     from pageable host memory, so the host waits until the copy has been
+ *     staged) and launches on the same stream.  Nothing in the array has to
+ *     start at zero: each call writes every field its launch reads.
+ *   - The array and the host staging are shared by all calls: calls that
+ *     overlap in time (several host threads, or streams not ordered with one
+ *     another) race.  Issue them from one thread on one stream, or order them. */
+#define FO_STATIC_MAX_TENSORS 1024
+fo_status fo_adamw_step_static(const fo_tensor* tensors, int n_tensors, fo_dtype grad_dtype, double lr,
+                               double beta1, double beta2, double eps, double weight_decay, int64_t step,
+                               int rho_bits, void* stream);
 
 #ifdef __cplusplus
 }

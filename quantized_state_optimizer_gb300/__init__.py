@@ -22,12 +22,14 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "FoError", "SPECS", "fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct",
-    "fo_adamw_step", "fo_max_tensors_per_launch", "fo_device_status", "FoTensor", "lib", "lib_path",
+    "fo_adamw_step", "fo_adamw_step_static", "FO_STATIC_MAX_TENSORS", "fo_max_tensors_per_launch",
+    "fo_device_status", "FoTensor", "lib", "lib_path",
 ]
 
 SPECS = {"momentum": 0, "variance": 1, "momentum_linear": 2, "variance_linear": 3}
 _SIGNED = {0: True, 1: False, 2: True, 3: False}
 FO_DT_F32, FO_DT_BF16 = 0, 1
+FO_STATIC_MAX_TENSORS = 1024  # include/fo.h
 
 
 class FoError(RuntimeError):
@@ -77,11 +79,13 @@ def lib() -> ctypes.CDLL:
         L.fo_split.argtypes = [p, i64, i32, p, p, p]
         L.fo_reconstruct.argtypes = [p, p, i64, i32, p, p]
         L.fo_adamw_step.argtypes = [ctypes.POINTER(FoTensor), i32, i32, d, d, d, d, d, i64, i32, p]
+        L.fo_adamw_step_static.argtypes = [ctypes.POINTER(FoTensor), i32, i32, d, d, d, d, d, i64, i32, p]
         L.fo_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.fo_device_status.restype = i32
         L.fo_max_tensors_per_launch.argtypes = []
         L.fo_max_tensors_per_launch.restype = i32
-        for f in ("fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct", "fo_adamw_step"):
+        for f in ("fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct", "fo_adamw_step",
+                  "fo_adamw_step_static"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -194,17 +198,30 @@ def make_fo_tensor(param: torch.Tensor, rho: torch.Tensor, grad: torch.Tensor, m
         n)
 
 
-def fo_adamw_step(tensors, grad_dtype, lr: float, beta1: float, beta2: float, eps: float,
-                  weight_decay: float, step: int, rho_bits: int, stream=None) -> None:
-    """One fused FlashAdamW step over a list of ``FoTensor`` (or a ctypes array of them)."""
+def _step_args(tensors, grad_dtype):
     if isinstance(grad_dtype, torch.dtype):
         grad_dtype = FO_DT_BF16 if grad_dtype == torch.bfloat16 else FO_DT_F32
     if isinstance(tensors, ctypes.Array):
-        arr, count = tensors, len(tensors)
-    else:
-        tensors = list(tensors)
-        count = len(tensors)
-        arr = (FoTensor * max(count, 1))(*tensors)
+        return tensors, len(tensors), int(grad_dtype)
+    tensors = list(tensors)
+    return (FoTensor * max(len(tensors), 1))(*tensors), len(tensors), int(grad_dtype)
+
+
+def fo_adamw_step(tensors, grad_dtype, lr: float, beta1: float, beta2: float, eps: float,
+                  weight_decay: float, step: int, rho_bits: int, stream=None) -> None:
+    """One fused FlashAdamW step over a list of ``FoTensor`` (or a ctypes array of them)."""
+    arr, count, gdt = _step_args(tensors, grad_dtype)
     _check("fo_adamw_step", lib().fo_adamw_step(
-        arr, count, int(grad_dtype), float(lr), float(beta1), float(beta2), float(eps),
+        arr, count, gdt, float(lr), float(beta1), float(beta2), float(eps),
+        float(weight_decay), int(step), int(rho_bits), _stream(stream)))
+
+
+def fo_adamw_step_static(tensors, grad_dtype, lr: float, beta1: float, beta2: float, eps: float,
+                         weight_decay: float, step: int, rho_bits: int, stream=None) -> None:
+    """``fo_adamw_step`` for at most ``FO_STATIC_MAX_TENSORS`` tensors in one
+    launch, with the list in the library's fixed device array: the call
+    allocates nothing (see include/fo.h for its set-up and sharing rules)."""
+    arr, count, gdt = _step_args(tensors, grad_dtype)
+    _check("fo_adamw_step_static", lib().fo_adamw_step_static(
+        arr, count, gdt, float(lr), float(beta1), float(beta2), float(eps),
         float(weight_decay), int(step), int(rho_bits), _stream(stream)))

@@ -243,6 +243,7 @@ const char* fo_status_string(fo_status s) {
     case FO_ERR_MISALIGNED: return "FO_ERR_MISALIGNED";
     case FO_ERR_CUDA: return "FO_ERR_CUDA";
     case FO_ERR_ALIAS: return "FO_ERR_ALIAS";
+    case FO_ERR_TOO_LARGE: return "FO_ERR_TOO_LARGE";
   }
   return "FO_ERR_UNKNOWN";
 }

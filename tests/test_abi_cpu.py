@@ -113,3 +113,22 @@ def test_step_alias_detection(L):
     # scales too short to hold ceil(n/32) entries overlap the next buffer
     d = _t(base, 1000, stride=32)
     assert _step(L, [d]) == ALIAS
+
+
+def test_static_step_host_checks(L):
+    """fo_adamw_step_static: the size limit comes first, then the same argument
+    and alias checks as fo_adamw_step, all before any CUDA call."""
+    big = (fo.FoTensor * (fo.FO_STATIC_MAX_TENSORS + 1))()
+    assert L.fo_adamw_step_static(big, len(big), 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8, None) == 5
+    assert L.fo_status_string(5) == b"FO_ERR_TOO_LARGE"
+    t = _t(1 << 32, 1000)
+    arr = (fo.FoTensor * 1)(t)
+    assert L.fo_adamw_step_static(arr, 1, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 0, 8, None) == INVALID
+    mis = _t(1 << 32, 1000)
+    mis.v_scales += 2
+    assert L.fo_adamw_step_static((fo.FoTensor * 1)(mis), 1, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8, None) == MISALIGNED
+    a = _t(1 << 32, 1000)
+    b = _t((1 << 32) + (1 << 24), 1000)
+    b.param = a.param + 512
+    assert L.fo_adamw_step_static((fo.FoTensor * 2)(a, b), 2, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8, None) == ALIAS
+    assert L.fo_adamw_step_static(None, 0, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8, None) == OK
