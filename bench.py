@@ -299,6 +299,23 @@ def cpu_baseline(sample_params: int, steps: int) -> dict:
 
 
 # ------------------------------------------------------------ main
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's step time: every rank must have finished a step for
+    the job to have finished it (a no-op outside torch.distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(params_per_rank: int, world_size: int, ms: float) -> float:
+    """Parameters the whole job steps per second: each rank steps its own list
+    (weak scaling), the job takes as long as its slowest rank."""
+    return world_size * params_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -355,13 +372,9 @@ def main():
     stream = torch.cuda.Stream(device=device)
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(st, args.steps, args.warmup, stream, dist_on)
-    ms = total_ms / args.steps
-    if dist_on:
-        tt = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(total_ms / args.steps, device)
     n = sum(numels)
-    value = ws * n / (ms * 1e-3)
+    value = job_throughput(n, ws, ms)
     bytes_step = algorithmic_bytes(numels)
     kernel_ms = statistics.mean(per)
     peak, peak_kind = load_peak()
