@@ -241,12 +241,13 @@ def time_e2e(st, numels, steps: int, stream) -> dict:
 
 
 # ------------------------------------------------------------ CPU oracle
-def oracle_sample(total_params: int, chunk: int = 1 << 20, seed: int = 1):
+def oracle_sample(total_params: int, chunk: int = 1 << 20, seed: int = 1, layers: int = 2):
     """A bounded, seeded sample of the workload for the CPU oracle: group-aligned
-    chunks of the first layer's tensors (each group is independent, so any
-    group-aligned piece is a valid unit of the step)."""
+    chunks of the first decoder layers' tensors (each group is independent, so
+    any group-aligned piece is a valid unit of the step)."""
     import oracle as O
-    specs = [s for s in W.llama_tensor_list(MODEL) if s.name.startswith("layers.0.")]
+    keep = tuple(f"layers.{i}." for i in range(layers))
+    specs = [s for s in W.llama_tensor_list(MODEL) if s.name.startswith(keep)]
     pieces = []
     left = total_params
     gen = torch.Generator().manual_seed(seed)
@@ -294,8 +295,9 @@ def cpu_baseline(sample_params: int, steps: int) -> dict:
     run_oracle_steps(pieces, 1, cores)  # first touch
     sec = run_oracle_steps(pieces, steps, cores, t0=2)
     return {"value": n * steps / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"{n:,} params of layer 0 of the {MODEL.name} list in group-aligned 1M-element pieces, "
-                       f"{steps} steps, one thread per piece on {cores} host cores")}
+            "seconds": sec,
+            "sample": (f"{n:,} params (decoder layers 0-1 of the {MODEL.name} list) in group-aligned "
+                       f"1M-element pieces, {steps} steps, one thread per piece on {cores} host cores")}
 
 
 # ------------------------------------------------------------ main
@@ -330,7 +332,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-sample", type=int, default=96 << 20)
+    ap.add_argument("--cpu-sample", type=int, default=436_224_000,
+                    help="parameters of the CPU-oracle sample (default: two decoder layers, ~10 s of work)")
+    ap.add_argument("--cpu-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: restrict to the first N decoder layers' tensors")
@@ -392,7 +396,7 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.cpu_sample, 3)
+        cpu = cpu_baseline(args.cpu_sample, args.cpu_steps)
     cfg = workload_config(numels)
     if args.layers is not None:
         cfg["workload"] = f"PROFILING SUBSET (first {args.layers} layers) of " + cfg["workload"]
