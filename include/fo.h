@@ -148,6 +148,51 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
                         double beta1, double beta2, double eps, double weight_decay, int64_t step,
                         int rho_bits, void* stream);
 
+/* ---- the step in the ablation formats ------------------------------------
+ * "code/flashsim/flash_adamw_sim.py", `FlashAdamWSim` with its ablation
+ * switches: `master_weight_bits` in {24, 32, None}, an fp32 parameter,
+ * `companded` and `quantize_states`.  Same update as fo_adamw_step (Algorithm
+ * 4, scalars formed in double and rounded once), in any combination of:
+ *   parameter  FO_PARAM_BF16_RHO8   bf16 theta' + int8 rho (24-bit master)
+ *              FO_PARAM_BF16_RHO16  bf16 theta' + int16 rho (32-bit master)
+ *              FO_PARAM_BF16        bf16 parameter, no split (master_weight_bits
+ *                                   None): theta = the parameter, written back
+ *                                   rounded to nearest even
+ *              FO_PARAM_F32         fp32 parameter, no split
+ *   states     FO_STATE_COMPANDED   MOMENTUM / VARIANCE specs (as fo_adamw_step)
+ *              FO_STATE_LINEAR      MOMENTUM_LINEAR / VARIANCE_LINEAR specs:
+ *                                   plain group-32 absmax codes of m and of v
+ *              FO_STATE_F32         fp32 m and v, no scales (quantize_states
+ *                                   False)
+ * Every result is the exact binary32 definition (the kernel evaluates the IEEE
+ * chain, with no approximation).  fo_adamw_step is the fast path for the two
+ * FO_PARAM_BF16_RHO* formats with FO_STATE_COMPANDED and gives the same bits.
+ * Buffers as in fo_tensor, with widths by format: param 2 or 4 bytes per
+ * element, rho 1 or 2 (unused, may be NULL, without a split), m and v 1 byte
+ * (codes) or 4 (fp32), m_scales / v_scales fp16 [ceil(numel/32)] (unused, may
+ * be NULL, for fp32 states).  All 16-byte aligned.  Same errors as
+ * fo_adamw_step. */
+typedef enum {
+  FO_PARAM_BF16_RHO8 = 0,
+  FO_PARAM_BF16_RHO16 = 1,
+  FO_PARAM_BF16 = 2,
+  FO_PARAM_F32 = 3
+} fo_param_format;
+typedef enum { FO_STATE_COMPANDED = 0, FO_STATE_LINEAR = 1, FO_STATE_F32 = 2 } fo_state_format;
+typedef struct {
+  void* param;
+  void* rho;
+  const void* grad;
+  void* m;
+  uint16_t* m_scales;
+  void* v;
+  uint16_t* v_scales;
+  int64_t numel;
+} fo_tensor_general;
+fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
+                                fo_state_format state_format, fo_dtype grad_dtype, double lr, double beta1,
+                                double beta2, double eps, double weight_decay, int64_t step, void* stream);
+
 /* Largest tensor list fo_adamw_step handles in a single kernel launch. */
 int fo_max_tensors_per_launch(void);
 

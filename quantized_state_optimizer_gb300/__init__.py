@@ -22,7 +22,8 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "FoError", "SPECS", "fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct",
-    "fo_adamw_step", "fo_adamw_step_static", "FO_STATIC_MAX_TENSORS", "fo_max_tensors_per_launch",
+    "fo_adamw_step", "fo_adamw_step_static", "FO_STATIC_MAX_TENSORS", "fo_adamw_step_general",
+    "FoTensorGeneral", "PARAM_FORMATS", "STATE_FORMATS", "fo_max_tensors_per_launch",
     "fo_device_status", "FoTensor", "lib", "lib_path",
 ]
 
@@ -30,6 +31,9 @@ SPECS = {"momentum": 0, "variance": 1, "momentum_linear": 2, "variance_linear": 
 _SIGNED = {0: True, 1: False, 2: True, 3: False}
 FO_DT_F32, FO_DT_BF16 = 0, 1
 FO_STATIC_MAX_TENSORS = 1024  # include/fo.h
+# fo_param_format / fo_state_format of include/fo.h
+PARAM_FORMATS = {"bf16_rho8": 0, "bf16_rho16": 1, "bf16": 2, "f32": 3}
+STATE_FORMATS = {"companded": 0, "linear": 1, "f32": 2}
 
 
 class FoError(RuntimeError):
@@ -48,6 +52,20 @@ class FoTensor(ctypes.Structure):
         ("m_codes", ctypes.c_void_p),
         ("m_scales", ctypes.c_void_p),
         ("v_codes", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+        ("numel", ctypes.c_int64),
+    ]
+
+
+class FoTensorGeneral(ctypes.Structure):
+    """``fo_tensor_general`` of include/fo.h: one tensor's buffers in any format."""
+    _fields_ = [
+        ("param", ctypes.c_void_p),
+        ("rho", ctypes.c_void_p),
+        ("grad", ctypes.c_void_p),
+        ("m", ctypes.c_void_p),
+        ("m_scales", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
         ("v_scales", ctypes.c_void_p),
         ("numel", ctypes.c_int64),
     ]
@@ -80,12 +98,14 @@ def lib() -> ctypes.CDLL:
         L.fo_reconstruct.argtypes = [p, p, i64, i32, p, p]
         L.fo_adamw_step.argtypes = [ctypes.POINTER(FoTensor), i32, i32, d, d, d, d, d, i64, i32, p]
         L.fo_adamw_step_static.argtypes = [ctypes.POINTER(FoTensor), i32, i32, d, d, d, d, d, i64, i32, p]
+        L.fo_adamw_step_general.argtypes = [ctypes.POINTER(FoTensorGeneral), i32, i32, i32, i32, d, d, d, d, d,
+                                            i64, p]
         L.fo_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.fo_device_status.restype = i32
         L.fo_max_tensors_per_launch.argtypes = []
         L.fo_max_tensors_per_launch.restype = i32
         for f in ("fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct", "fo_adamw_step",
-                  "fo_adamw_step_static"):
+                  "fo_adamw_step_static", "fo_adamw_step_general"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -225,3 +245,22 @@ def fo_adamw_step_static(tensors, grad_dtype, lr: float, beta1: float, beta2: fl
     _check("fo_adamw_step_static", lib().fo_adamw_step_static(
         arr, count, gdt, float(lr), float(beta1), float(beta2), float(eps),
         float(weight_decay), int(step), int(rho_bits), _stream(stream)))
+
+
+def fo_adamw_step_general(tensors, param_format, state_format, grad_dtype, lr: float, beta1: float,
+                          beta2: float, eps: float, weight_decay: float, step: int, stream=None) -> None:
+    """The step in any parameter / state format (``PARAM_FORMATS``, ``STATE_FORMATS``)
+    over a list of ``FoTensorGeneral`` (or a ctypes array of them)."""
+    if isinstance(grad_dtype, torch.dtype):
+        grad_dtype = FO_DT_BF16 if grad_dtype == torch.bfloat16 else FO_DT_F32
+    pf = PARAM_FORMATS[param_format] if isinstance(param_format, str) else int(param_format)
+    sf = STATE_FORMATS[state_format] if isinstance(state_format, str) else int(state_format)
+    if isinstance(tensors, ctypes.Array):
+        arr, count = tensors, len(tensors)
+    else:
+        tensors = list(tensors)
+        count = len(tensors)
+        arr = (FoTensorGeneral * max(count, 1))(*tensors)
+    _check("fo_adamw_step_general", lib().fo_adamw_step_general(
+        arr, count, pf, sf, int(grad_dtype), float(lr), float(beta1), float(beta2), float(eps),
+        float(weight_decay), int(step), _stream(stream)))

@@ -27,4 +27,13 @@ inline fo_status launch_status() {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Python-float scalars of the AdamW update, each formed in double and rounded
+// once to fp32 (as torch does for scalar operands of fp32 tensor arithmetic).
+struct StepScalars {
+  float c_wd, b1, one_minus_b1, b2, one_minus_b2, bc1, bc2, lr, eps;
+  // constants of the approximate update: RN(lr * RN(1/bc1)) and RN(sqrt(RN(1/bc2)))
+  float lr_ib1, sqrt_ib2;
+};
+StepScalars step_scalars(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
+
 }  // namespace fo

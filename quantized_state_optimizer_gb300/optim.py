@@ -192,15 +192,44 @@ class FlashAdamW(torch.optim.Optimizer):
     rho) or 32 (int16 rho).  Gradients may be bf16 or fp32 (one dtype per
     step call).  All parameters of all groups that have a gradient are updated
     by one launch per param group.
+
+    ``gradient_release=True`` steps each parameter inside backward instead:
+    a post-accumulate-grad hook launches the single-tensor step as soon as
+    the parameter's gradient is complete and then frees the gradient, so no
+    gradient outlives its own update (the ``gradient_release`` accounting of
+    ``bytes_per_param`` on the page "code/flashsim/flash_adamw_sim.py").
+    ``step()`` is then a no-op for those parameters.  The result equals a
+    normal step on the same gradients bit for bit: every tensor's update is
+    independent of the others.
     """
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0,
-                 master_weight_bits: int = 24):
+                 master_weight_bits: int = 24, gradient_release: bool = False):
         if master_weight_bits not in (24, 32):
             raise ValueError("master_weight_bits must be 24 or 32")
         defaults = dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay)
         super().__init__(params, defaults)
         self.rho_bits = 8 if master_weight_bits == 24 else 16
+        self.gradient_release = gradient_release
+        self._hooks = []
+        if gradient_release:
+            for group in self.param_groups:
+                for p in group["params"]:
+                    self._hooks.append(p.register_post_accumulate_grad_hook(self._release_hook(group)))
+
+    def _release_hook(self, group):
+        def hook(p: torch.Tensor) -> None:
+            with torch.no_grad():
+                self._step_params(group, [p])
+            p.grad = None
+        return hook
+
+    def remove_hooks(self) -> None:
+        """Detach the gradient-release hooks (the optimizer then steps in ``step()``)."""
+        for h in self._hooks:
+            h.remove()
+        self._hooks = []
+        self.gradient_release = False
 
     def _init_state(self, p: torch.Tensor) -> dict:
         if p.dtype != torch.bfloat16 or not p.is_cuda or not p.is_contiguous():
@@ -223,24 +252,29 @@ class FlashAdamW(torch.optim.Optimizer):
         if closure is not None:
             with torch.enable_grad():
                 loss = closure()
-        for group in self.param_groups:
-            beta1, beta2 = group["betas"]
-            by_key: dict[tuple[int, torch.dtype], list] = {}
-            for p in group["params"]:
-                if p.grad is None:
-                    continue
-                st = self.state[p]
-                if len(st) == 0:
-                    st = self._init_state(p)
-                st["step"] += 1
-                g = p.grad
-                if not g.is_contiguous():
-                    g = g.contiguous()
-                ft = FoTensor(p.data_ptr(), st["rho"].data_ptr(), g.data_ptr(), st["m_codes"].data_ptr(),
-                              st["m_scales"].data_ptr(), st["v_codes"].data_ptr(),
-                              st["v_scales"].data_ptr(), p.numel())
-                by_key.setdefault((st["step"], g.dtype), []).append((ft, g))
-            for (t, gdt), items in by_key.items():
-                fo_adamw_step([ft for ft, _ in items], gdt, group["lr"], beta1, beta2, group["eps"],
-                              group["weight_decay"], t, self.rho_bits)
+        if not self.gradient_release:
+            for group in self.param_groups:
+                self._step_params(group, group["params"])
         return loss
+
+    def _step_params(self, group, params) -> None:
+        """One launch per (step count, grad dtype) over the parameters that have a gradient."""
+        beta1, beta2 = group["betas"]
+        by_key: dict[tuple[int, torch.dtype], list] = {}
+        for p in params:
+            if p.grad is None:
+                continue
+            st = self.state[p]
+            if len(st) == 0:
+                st = self._init_state(p)
+            st["step"] += 1
+            g = p.grad
+            if not g.is_contiguous():
+                g = g.contiguous()
+            ft = FoTensor(p.data_ptr(), st["rho"].data_ptr(), g.data_ptr(), st["m_codes"].data_ptr(),
+                          st["m_scales"].data_ptr(), st["v_codes"].data_ptr(),
+                          st["v_scales"].data_ptr(), p.numel())
+            by_key.setdefault((st["step"], g.dtype), []).append((ft, g))
+        for (t, gdt), items in by_key.items():
+            fo_adamw_step([ft for ft, _ in items], gdt, group["lr"], beta1, beta2, group["eps"],
+                          group["weight_decay"], t, self.rho_bits)

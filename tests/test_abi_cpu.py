@@ -132,3 +132,19 @@ def test_static_step_host_checks(L):
     b.param = a.param + 512
     assert L.fo_adamw_step_static((fo.FoTensor * 2)(a, b), 2, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8, None) == ALIAS
     assert L.fo_adamw_step_static(None, 0, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 8, None) == OK
+
+
+def test_general_step_host_checks(L):
+    """fo_adamw_step_general rejects bad formats and arguments before any CUDA call."""
+    t = fo.FoTensorGeneral(1 << 32, 0, (1 << 32) + (2 << 20), (1 << 32) + (3 << 20), 0,
+                           (1 << 32) + (5 << 20), 0, 1000)
+    arr = (fo.FoTensorGeneral * 1)(t)
+    call = lambda pf, sf, **kw: L.fo_adamw_step_general(  # noqa: E731
+        arr, 1, pf, sf, kw.get("gd", 1), 1e-3, 0.9, 0.999, 1e-8, 0.0, kw.get("step", 1), None)
+    assert call(4, 0) == INVALID          # no such parameter format
+    assert call(0, 3) == INVALID          # no such state format
+    assert call(3, 2, gd=7) == INVALID    # no such grad dtype
+    assert call(3, 2, step=0) == INVALID
+    assert call(0, 2) == INVALID          # a split needs rho
+    assert call(3, 0) == INVALID          # quantized states need scales
+    assert L.fo_adamw_step_general(None, 0, 3, 2, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None) == OK

@@ -1,0 +1,158 @@
+"""The step in the ablation formats (fo_adamw_step_general) against the CPU
+oracle, bit for bit: every parameter format (24- and 32-bit masters, a bf16
+parameter without a split, an fp32 parameter) with every state format
+(companded codes, linear codes, fp32 states), fp32 and bf16 gradients, over a
+ragged list and several steps.  And in the paper's own format, the general
+kernel gives the same bits as the fast one."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import quantized_state_optimizer_gb300 as fo
+import workloads as W
+from quantized_state_optimizer_gb300 import FoTensorGeneral
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+NUMELS = [1, 33, 4096 + 17, 12345, 0, 64]
+
+
+def _theta(i, n):
+    g = torch.Generator().manual_seed(300 + i)
+    return (torch.randn(n, generator=g) * 0.02).float()
+
+
+def _grad(i, t, n, dtype):
+    g = torch.Generator().manual_seed(W.grad_seed(55, i, t))
+    x = torch.randn(n, generator=g) * torch.exp(torch.randn(n, generator=g)) * 1e-3
+    return x if dtype == torch.float32 else x.to(torch.bfloat16)
+
+
+class DevTensor:
+    """Device buffers of one tensor in the given formats, initialised from theta."""
+
+    def __init__(self, theta, pf, sf, grad_dtype):
+        n = theta.numel()
+        self.n, self.pf, self.sf = n, pf, sf
+        t = theta.to(DEV)
+        if pf in ("bf16_rho8", "bf16_rho16"):
+            rb = 8 if pf == "bf16_rho8" else 16
+            self.param = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+            self.rho = torch.empty(n, dtype=torch.int8 if rb == 8 else torch.int16, device=DEV)
+            if n:
+                fo.fo_split(t, rb, self.param, self.rho)
+        elif pf == "bf16":
+            self.param, self.rho = t.to(torch.bfloat16), None
+        else:
+            self.param, self.rho = t.clone(), None
+        if sf == "f32":
+            self.m = torch.zeros(n, dtype=torch.float32, device=DEV)
+            self.v = torch.zeros(n, dtype=torch.float32, device=DEV)
+            self.ms = self.vs = None
+        else:
+            self.m = torch.zeros(n, dtype=torch.int8, device=DEV)
+            self.v = torch.zeros(n, dtype=torch.uint8, device=DEV)
+            self.ms = torch.zeros((n + 31) // 32, dtype=torch.float16, device=DEV)
+            self.vs = torch.zeros((n + 31) // 32, dtype=torch.float16, device=DEV)
+        self.grad = torch.zeros(n, dtype=grad_dtype, device=DEV)
+
+    def ft(self):
+        p = lambda x: x.data_ptr() if x is not None else None  # noqa: E731
+        return FoTensorGeneral(p(self.param), p(self.rho), p(self.grad), p(self.m), p(self.ms), p(self.v),
+                               p(self.vs), self.n)
+
+    def host(self):
+        def bits(x):
+            if x is None:
+                return None
+            x = x.cpu()
+            if x.dtype in (torch.bfloat16, torch.float16):
+                return x.view(torch.int16).numpy().view(np.uint16)
+            return x.numpy()
+        return {k: bits(getattr(self, k)) for k in ("param", "rho", "m", "ms", "v", "vs")}
+
+
+def _oracle_state(theta, pf, sf):
+    qs = sf != "f32"
+    if pf == "f32":
+        return O.TensorState.init(theta.numpy(), quantize_states=qs, param_dtype="f32")
+    mb = {"bf16_rho8": 24, "bf16_rho16": 32, "bf16": None}[pf]
+    return O.TensorState.init(theta.numpy(), master_bits=mb, quantize_states=qs)
+
+
+def _same(a, b, ctx):
+    if a is None and (b is None or b.size == 0):
+        return
+    a, b = np.asarray(a), np.asarray(b)
+    assert a.shape == b.shape, ctx
+    if a.dtype == np.float32:
+        a, b = a.view(np.uint32), b.view(np.uint32)
+    bad = np.flatnonzero(a != b)
+    assert bad.size == 0, f"{ctx}: {bad.size} of {a.size} differ (first {bad[:5]})"
+
+
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("sf", ["companded", "linear", "f32"])
+@pytest.mark.parametrize("pf", ["bf16_rho8", "bf16_rho16", "bf16", "f32"])
+def test_general_step_matches_oracle(pf, sf, grad_dtype):
+    h = W.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.05, steps=3)
+    thetas = [_theta(i, n) for i, n in enumerate(NUMELS)]
+    dev = [DevTensor(t, pf, sf, grad_dtype) for t in thetas]
+    refs = [_oracle_state(t, pf, sf) for t in thetas]
+    arr = (FoTensorGeneral * len(dev))(*[d.ft() for d in dev])
+    for t in range(1, h.steps + 1):
+        for i, n in enumerate(NUMELS):
+            if n == 0:
+                continue
+            g = _grad(i, t, n, grad_dtype)
+            dev[i].grad.copy_(g.to(DEV))
+            gn = g.numpy() if grad_dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16)
+            O.adamw_step(refs[i], gn, t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay,
+                         quantize_states=sf != "f32", companded=sf == "companded")
+        fo.fo_adamw_step_general(arr, pf, sf, grad_dtype, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, t)
+        torch.cuda.synchronize()
+        for i, n in enumerate(NUMELS):
+            if n == 0:
+                continue
+            got, r = dev[i].host(), refs[i]
+            ctx = (pf, sf, str(grad_dtype), i, t)
+            _same(got["param"], r.param, ctx + ("param",))
+            if r.rho is not None:
+                _same(got["rho"], r.rho, ctx + ("rho",))
+            _same(got["m"], r.m, ctx + ("m",))
+            _same(got["v"], r.v, ctx + ("v",))
+            if sf != "f32":
+                _same(got["ms"], r.m_scales, ctx + ("m_scales",))
+                _same(got["vs"], r.v_scales, ctx + ("v_scales",))
+
+
+@pytest.mark.parametrize("rho_bits", [8, 16])
+def test_general_kernel_equals_fast_kernel_in_the_papers_format(rho_bits):
+    from quantized_state_optimizer_gb300.optim import FlashAdamWState
+    numels = [70000, 4096 * 5 + 3, 31]
+    h = W.LLAMA3_8B_HYPER
+    st = FlashAdamWState(numels, rho_bits=rho_bits, grad_dtype=torch.bfloat16, device=DEV)
+    pf = "bf16_rho8" if rho_bits == 8 else "bf16_rho16"
+    gen = []
+    for i, n in enumerate(numels):
+        th = _theta(i, n)
+        st.init_theta(i, th.to(DEV))
+        gen.append(DevTensor(th, pf, "companded", torch.bfloat16))
+    arr = (FoTensorGeneral * len(gen))(*[d.ft() for d in gen])
+    for t in (1, 2, 3):
+        for i, n in enumerate(numels):
+            g = _grad(i, t, n, torch.bfloat16).to(DEV)
+            st.grad_view(i).copy_(g)
+            gen[i].grad.copy_(g)
+        st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        fo.fo_adamw_step_general(arr, pf, "companded", torch.bfloat16, h.lr, h.beta1, h.beta2, h.eps,
+                                 h.weight_decay, t)
+        torch.cuda.synchronize()
+        for i in range(len(numels)):
+            v = st.view(i)
+            d = gen[i]
+            for a, b in ((v["param"], d.param), (v["rho"], d.rho), (v["m_codes"], d.m), (v["v_codes"], d.v),
+                         (v["m_scales"], d.ms), (v["v_scales"], d.vs)):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (i, t)

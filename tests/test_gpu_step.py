@@ -325,3 +325,35 @@ def test_llama_1b_list_int16_rho_20_steps_sampled():
 def test_llama3_8b_list_int8_rho_20_steps_sampled():
     st = run_full_size(W.LLAMA3_8B, W.LLAMA3_8B_HYPER, W.LLAMA3_8B_MASTER_BITS, groups_per_tensor=16)
     assert st.total_numel() == 8_030_261_248 and len(st) == 291
+
+
+def test_gradient_release_matches_step():
+    """FlashAdamW(gradient_release=True) steps each parameter inside backward
+    and frees its gradient; parameters and states equal those of the normal
+    step on the same gradients, bit for bit."""
+    torch.manual_seed(0)
+
+    def model():
+        torch.manual_seed(0)
+        return torch.nn.Sequential(torch.nn.Linear(64, 96), torch.nn.GELU(), torch.nn.Linear(96, 48)).to(
+            device=DEV, dtype=torch.bfloat16)
+
+    a, b = model(), model()
+    opt_a = FlashAdamW(a.parameters(), lr=1e-3, weight_decay=0.1)
+    opt_b = FlashAdamW(b.parameters(), lr=1e-3, weight_decay=0.1, gradient_release=True)
+    for t in range(3):
+        x = torch.randn(32, 64, generator=torch.Generator().manual_seed(t)).to(DEV, torch.bfloat16)
+        (a(x).float() ** 2).mean().backward()
+        opt_a.step()
+        opt_a.zero_grad(set_to_none=True)
+        (b(x).float() ** 2).mean().backward()
+        assert all(p.grad is None for p in b.parameters())
+        opt_b.step()  # nothing left to do
+        torch.cuda.synchronize()
+        for pa, pb in zip(a.parameters(), b.parameters()):
+            assert torch.equal(pa.view(torch.int16), pb.view(torch.int16)), t
+            sa, sb = opt_a.state[pa], opt_b.state[pb]
+            assert sa["step"] == sb["step"] == t + 1
+            for k in ("rho", "m_codes", "m_scales", "v_codes", "v_scales"):
+                assert torch.equal(sa[k].view(torch.uint8), sb[k].view(torch.uint8)), (k, t)
+    opt_b.remove_hooks()
