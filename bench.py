@@ -166,19 +166,84 @@ def bench_specs(layers: int | None):
     return [s for s in specs if s.name.startswith(keep)]
 
 
-def build_state(device, layers: int | None = None):
+def build_state(device, layers: int | None = None, fmt: str | None = None):
     from quantized_state_optimizer_gb300.optim import FlashAdamWState
     all_specs = W.llama_tensor_list(MODEL)
     specs = bench_specs(layers)
     numels = [s.numel for s in specs]
     wid = W.WORKLOAD_IDS[MODEL.name]
-    st = FlashAdamWState(numels, rho_bits=RHO_BITS, grad_dtype=torch.bfloat16, device=device)
+    if fmt is not None:
+        st = GeneralState(numels, *fmt.split(":"), device)
+    else:
+        st = FlashAdamWState(numels, rho_bits=RHO_BITS, grad_dtype=torch.bfloat16, device=device)
     for i, s in enumerate(specs):
         k = all_specs.index(s)  # seeds follow the tensor's index in the full list
         st.init_theta(i, W.init_theta(s, wid, k, device))
         W.make_grad(s.numel, wid, k, 1, device, out=st.grad_view(i))
     torch.cuda.synchronize()
     return st, numels
+
+
+# ------------------------------------------------- the ablation formats
+def general_bytes_per_param(pf: str, sf: str) -> float:
+    """Algorithmic bytes of one step per parameter in a format (bf16 grads)."""
+    param = 4 if pf == "f32" else 2
+    rho = {"bf16_rho8": 1, "bf16_rho16": 2}.get(pf, 0)
+    states = 16.0 if sf == "f32" else 4.0 + 4 * 2 / 32
+    return 2 + 2 * param + 2 * rho + states
+
+
+class GeneralState:
+    """Flat device slabs of the list in one of the ablation formats, and the
+    ``fo_tensor_general`` array over them (for ``fo_adamw_step_general``)."""
+
+    def __init__(self, numels, pf: str, sf: str, device):
+        import quantized_state_optimizer_gb300 as fo
+        self.pf, self.sf = pf, sf
+        align = lambda n: (n + 15) // 16 * 16  # noqa: E731
+        offs, o = [], 0
+        for n in numels:
+            offs.append(o)
+            o += align(n)
+        goffs, go = [], 0
+        for n in numels:
+            goffs.append(go)
+            go += align((n + 31) // 32)
+        total, gtotal = max(o, 16), max(go, 16)
+        self.offs, self.numels = offs, numels
+        self.param = torch.zeros(total, dtype=torch.float32 if pf == "f32" else torch.bfloat16, device=device)
+        self.rho = (torch.zeros(total, dtype=torch.int8 if pf == "bf16_rho8" else torch.int16, device=device)
+                    if pf in ("bf16_rho8", "bf16_rho16") else None)
+        st_dt = (torch.float32, torch.float32) if sf == "f32" else (torch.int8, torch.uint8)
+        self.m = torch.zeros(total, dtype=st_dt[0], device=device)
+        self.v = torch.zeros(total, dtype=st_dt[1], device=device)
+        self.ms = None if sf == "f32" else torch.zeros(gtotal, dtype=torch.float16, device=device)
+        self.vs = None if sf == "f32" else torch.zeros(gtotal, dtype=torch.float16, device=device)
+        self.grad = torch.zeros(total, dtype=torch.bfloat16, device=device)
+        ptr = lambda t, off, esz: t.data_ptr() + off * esz if t is not None else None  # noqa: E731
+        self.arr = (fo.FoTensorGeneral * len(numels))(*[
+            fo.FoTensorGeneral(ptr(self.param, offs[i], self.param.element_size()),
+                               ptr(self.rho, offs[i], self.rho.element_size() if self.rho is not None else 0),
+                               ptr(self.grad, offs[i], 2), ptr(self.m, offs[i], self.m.element_size()),
+                               ptr(self.ms, goffs[i], 2), ptr(self.v, offs[i], self.v.element_size()),
+                               ptr(self.vs, goffs[i], 2), n)
+            for i, n in enumerate(numels)])
+
+    def init_theta(self, i: int, theta: torch.Tensor) -> None:
+        import quantized_state_optimizer_gb300 as fo
+        o, n = self.offs[i], self.numels[i]
+        if self.rho is not None:
+            fo.fo_split(theta, 8 if self.pf == "bf16_rho8" else 16, self.param[o:o + n], self.rho[o:o + n])
+        else:
+            self.param[o:o + n].copy_(theta)
+
+    def grad_view(self, i: int) -> torch.Tensor:
+        return self.grad[self.offs[i]:self.offs[i] + self.numels[i]]
+
+    def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
+        import quantized_state_optimizer_gb300 as fo
+        fo.fo_adamw_step_general(self.arr, self.pf, self.sf, torch.bfloat16, lr, beta1, beta2, eps,
+                                 weight_decay, t, stream)
 
 
 def time_steps(st, steps: int, warmup: int, stream, dist_on: bool) -> tuple[float, list[float]]:
@@ -338,6 +403,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: restrict to the first N decoder layers' tensors")
+    ap.add_argument("--format", default=None,
+                    help="PARAM:STATES, e.g. bf16:linear or f32:f32 -- time fo_adamw_step_general in an "
+                         "ablation format (parameter: bf16_rho8, bf16_rho16, bf16, f32; states: companded, "
+                         "linear, f32) instead of the fast step")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     numels = [s.numel for s in W.llama_tensor_list(MODEL)]
@@ -372,19 +441,20 @@ def main():
     import quantized_state_optimizer_gb300 as fo
     fo.lib()  # fail loudly if the CUDA library is missing
 
-    st, numels = build_state(device, args.layers)
+    st, numels = build_state(device, args.layers, args.format)
     stream = torch.cuda.Stream(device=device)
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(st, args.steps, args.warmup, stream, dist_on)
     ms = max_over_ranks(total_ms / args.steps, device)
     n = sum(numels)
     value = job_throughput(n, ws, ms)
-    bytes_step = algorithmic_bytes(numels)
+    bytes_step = (algorithmic_bytes(numels) if args.format is None
+                  else int(round(general_bytes_per_param(*args.format.split(":")) * sum(numels))))
     kernel_ms = statistics.mean(per)
     peak, peak_kind = load_peak()
     achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
     try:
-        e2e = time_e2e(st, numels, args.e2e_steps, stream) if args.e2e_steps > 0 else None
+        e2e = time_e2e(st, numels, args.e2e_steps, stream) if args.e2e_steps > 0 and args.format is None else None
     except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
         e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
     del st
@@ -400,6 +470,9 @@ def main():
     cfg = workload_config(numels)
     if args.layers is not None:
         cfg["workload"] = f"PROFILING SUBSET (first {args.layers} layers) of " + cfg["workload"]
+    if args.format is not None:
+        cfg["workload"] = (f"ABLATION FORMAT {args.format} (fo_adamw_step_general, exact chain) of the "
+                           f"{MODEL.name} list: {len(numels)} tensors, {sum(numels):,} params, bf16 grads")
     cfg["bytes_per_step"] = bytes_step
     cfg["bytes_per_param"] = bytes_step / n
     cfg["hbm_gbs"] = achieved
@@ -409,9 +482,9 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
-                     "kernel": "fo::adamw_step_kernel", "kernel_ms": kernel_ms,
-                     "bytes_per_launch": bytes_step,
-                     "traffic": captured_traffic(n) if args.layers is None else None},
+                     "kernel": "fo::adamw_step_kernel" if args.format is None else "fo::general_step_kernel",
+                     "kernel_ms": kernel_ms, "bytes_per_launch": bytes_step,
+                     "traffic": captured_traffic(n) if args.layers is None and args.format is None else None},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
