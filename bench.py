@@ -63,13 +63,13 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
 
 # DRAM bytes (read + write) per parameter of the step kernel, from one ncu
 # capture on layer 0 of the list (profiles/adamw_step_llama3_8b_layer0_ncu.md):
-# 1.554492 GB read + 1.062326 GB written for 218,112,000 parameters.  Traffic
+# 1.554265 GB read + 1.062396 GB written for 218,112,000 parameters.  Traffic
 # grows with the parameters processed, so a full launch is that figure times
 # the list's size.  It stands only for the kernel sources it was taken on.
 TRAFFIC_CAPTURE = {
-    "bytes_per_param": (1.554492e9 + 1.062326e9) / 218112000,
+    "bytes_per_param": (1.554265e9 + 1.062396e9) / 218112000,
     "sha256": {
-        "quantized_state_optimizer_gb300/csrc/fo_step.cu": "04ee2810840392f49cc3af905f089e8fa0ffa0a6d156bf5ed7f610fd7700963d",
+        "quantized_state_optimizer_gb300/csrc/fo_step.cu": "af6e7a328bc49b2fa33ca220ffe02c902560e529b54144a5555b675b3db29c01",
         "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
     },
 }
