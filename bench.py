@@ -359,8 +359,11 @@ def cpu_baseline(sample_params: int, steps: int) -> dict:
     n = sum(p[0].numel for p in pieces)
     run_oracle_steps(pieces, 1, cores)  # first touch
     sec = run_oracle_steps(pieces, steps, cores, t0=2)
+    # one thread, one step over the first 8 pieces: the oracle's serial speed
+    few = pieces[:8]
+    sec1 = run_oracle_steps(few, 1, 1, t0=steps + 2)
     return {"value": n * steps / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "seconds": sec,
+            "seconds": sec, "single_thread_value": sum(p[0].numel for p in few) / sec1,
             "sample": (f"{n:,} params (decoder layers 0-1 of the {MODEL.name} list) in group-aligned "
                        f"1M-element pieces, {steps} steps, one thread per piece on {cores} host cores")}
 
@@ -482,6 +485,7 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
+                     "frac_of_nominal_8000_gbs": achieved / 8000.0,
                      "kernel": "fo::adamw_step_kernel" if args.format is None else "fo::general_step_kernel",
                      "kernel_ms": kernel_ms, "bytes_per_launch": bytes_step,
                      "traffic": captured_traffic(n) if args.layers is None and args.format is None else None},
