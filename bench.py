@@ -368,6 +368,37 @@ def cpu_baseline(sample_params: int, steps: int) -> dict:
                        f"1M-element pieces, {steps} steps, one thread per piece on {cores} host cores")}
 
 
+# ------------------------------------------------------------ host link
+def host_link(gib: int = 8) -> dict:
+    """Pinned host <-> device copy bandwidth (GB/s) on 2*gib GB buffers, one
+    direction at a time and both at once: the ceiling of the e2e number."""
+    n = gib << 30
+    h = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    h2 = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    d = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    d2 = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        fn()
+        torch.cuda.synchronize()
+        return time.perf_counter() - t
+
+    def both():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    timed(lambda: d.copy_(h, non_blocking=True))
+    gb = n * 2 / 1e9
+    return {"h2d_gbs": gb / timed(lambda: d.copy_(h, non_blocking=True)),
+            "d2h_gbs": gb / timed(lambda: h2.copy_(d, non_blocking=True)),
+            "both_directions_gbs": 2 * gb / timed(both), "bytes_each": int(n * 2)}
+
+
 # ------------------------------------------------------------ main
 def max_over_ranks(ms: float, device) -> float:
     """The slowest rank's step time: every rank must have finished a step for
@@ -406,6 +437,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: restrict to the first N decoder layers' tensors")
+    ap.add_argument("--host-link", action="store_true",
+                    help="only measure pinned host <-> device copy bandwidth and print it as JSON")
     ap.add_argument("--format", default=None,
                     help="PARAM:STATES, e.g. bf16:linear or f32:f32 -- time fo_adamw_step_general in an "
                          "ablation format (parameter: bf16_rho8, bf16_rho16, bf16, f32; states: companded, "
@@ -434,6 +467,10 @@ def main():
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "gpu_launches": 0}
         print(json.dumps(line), flush=True)
+        return
+
+    if args.host_link:
+        print(json.dumps({"host_link": host_link()}), flush=True)
         return
 
     dist_on = ws > 1
