@@ -85,6 +85,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.fo_oracle_adamw_step.argtypes = [i64, p, i32, p, p, i32, p, p, p, p, i32, i32,
                                        d, d, d, d, d, i64]
     L.fo_oracle_adamw_step.restype = i32
+    L.fo_oracle_sgd_step.argtypes = [i64, p, i32, p, p, i32, p, p, i32, i32, d, d, d]
+    L.fo_oracle_sgd_step.restype = i32
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -246,6 +248,27 @@ def adamw_step(st: TensorState, grad, step: int, lr: float, beta1: float, beta2:
         int(quantize_states), int(companded), lr, beta1, beta2, eps, weight_decay, step)
     if rc != 0:
         raise RuntimeError("oracle adamw_step failed")
+
+
+def sgd_step(st: TensorState, grad, lr: float, momentum: float, weight_decay: float,
+             quantize_states: bool = True, companded: bool = True) -> None:
+    """One FlashSGD step of one tensor, in place (the momentum buffer lives in
+    ``st.m`` / ``st.m_scales``; ``st.v`` is unused).  ``grad`` is fp32 or bf16
+    bits (uint16).  The update is the reading stated in fo_oracle.h [B]."""
+    grad = np.ascontiguousarray(np.asarray(grad).reshape(-1))
+    if grad.dtype == np.float32:
+        gk = GRAD_F32
+    elif grad.dtype == np.uint16:
+        gk = GRAD_BF16
+    else:
+        raise TypeError(f"grad dtype {grad.dtype}")
+    assert grad.size == st.numel
+    rc = lib().fo_oracle_sgd_step(
+        st.numel, _ptr(st.param), st.param_kind, _ptr(st.rho) if st.rho is not None else 0,
+        _ptr(grad), gk, _ptr(st.m), _ptr(st.m_scales) if st.m_scales.size else 0,
+        int(quantize_states), int(companded), lr, momentum, weight_decay)
+    if rc != 0:
+        raise RuntimeError("oracle sgd_step failed")
 
 
 # ------------------------------------------------------------ statistics

@@ -340,3 +340,54 @@ int fo_oracle_adamw_step(int64_t n, void* param, int param_kind, void* rho, cons
   free(g); free(m); free(v); free(theta);
   return 0;
 }
+
+/* One FlashSGD step (the reading stated in fo_oracle.h [B]). */
+int fo_oracle_sgd_step(int64_t n, void* param, int param_kind, void* rho, const void* grad, int grad_kind,
+                       void* m_state, uint16_t* m_scales, int quantize_states, int companded, double lr,
+                       double momentum, double weight_decay) {
+  if (n < 0) return -1;
+  if (param_kind < 0 || param_kind > 3 || (grad_kind != 0 && grad_kind != 1)) return -1;
+  if (n == 0) return 0;
+  size_t bytes = (size_t)n * sizeof(float);
+  float* g = (float*)malloc(bytes);
+  float* buf = (float*)malloc(bytes);
+  float* theta = (float*)malloc(bytes);
+  if (!g || !buf || !theta) {
+    free(g); free(buf); free(theta);
+    return -1;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    if (grad_kind == FO_ORACLE_GRAD_F32) g[i] = ((const float*)grad)[i];
+    else g[i] = float_of((uint32_t)((const uint16_t*)grad)[i] << 16);
+  }
+  /* prologue: the momentum buffer and the master weight */
+  if (quantize_states) fo_oracle_dequantize(m_state, m_scales, n, 1, 0, companded ? 1 : 0, buf);
+  else memcpy(buf, m_state, bytes);
+  if (param_kind == FO_ORACLE_PARAM_BF16_RHO8 || param_kind == FO_ORACLE_PARAM_BF16_RHO16) {
+    fo_oracle_reconstruct((const uint16_t*)param, rho, n, param_kind == FO_ORACLE_PARAM_BF16_RHO8 ? 24 : 32, theta);
+  } else if (param_kind == FO_ORACLE_PARAM_BF16) {
+    for (int64_t i = 0; i < n; ++i) theta[i] = float_of((uint32_t)((uint16_t*)param)[i] << 16);
+  } else {
+    memcpy(theta, param, bytes);
+  }
+  /* Python-float scalars, rounded once to binary32 */
+  const float lr_f = (float)lr, mu = (float)momentum, wd = (float)weight_decay;
+  for (int64_t i = 0; i < n; ++i) {
+    float gi = g[i];
+    if (weight_decay != 0.0) gi = gi + wd * theta[i];
+    buf[i] = mu * buf[i] + gi;
+    theta[i] = theta[i] - lr_f * buf[i];
+  }
+  /* epilogue */
+  if (quantize_states) fo_oracle_quantize(buf, n, 1, 0, companded ? 1 : 0, m_state, m_scales);
+  else memcpy(m_state, buf, bytes);
+  if (param_kind == FO_ORACLE_PARAM_BF16_RHO8 || param_kind == FO_ORACLE_PARAM_BF16_RHO16) {
+    fo_oracle_split(theta, n, param_kind == FO_ORACLE_PARAM_BF16_RHO8 ? 24 : 32, (uint16_t*)param, rho);
+  } else if (param_kind == FO_ORACLE_PARAM_BF16) {
+    fo_oracle_f32_to_bf16_rne_array(theta, n, (uint16_t*)param);
+  } else {
+    memcpy(param, theta, bytes);
+  }
+  free(g); free(buf); free(theta);
+  return 0;
+}

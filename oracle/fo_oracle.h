@@ -78,6 +78,23 @@ int fo_oracle_adamw_step(int64_t n, void* param, int param_kind, void* rho, cons
                          uint16_t* v_scales, int quantize_states, int companded, double lr,
                          double beta1, double beta2, double eps, double weight_decay, int64_t step);
 
+/* ---- [B] one FlashSGD step on one tensor ------------------------------- */
+/* The pages name FlashSGD only in the byte accounting of
+ * "code/flashsim/flash_adamw_sim.py" (`bytes_per_param`: the master weight
+ * split as in FlashAdamW and one quantized state, the momentum).  The update
+ * read here is SGD with momentum as in torch.optim.SGD (dampening 0, no
+ * Nesterov, weight decay added to the gradient), every operation rounded
+ * once:
+ *   g = fp32(grad); if wd != 0: g = g + wd * theta;
+ *   buf = momentum * buf + g;  theta = theta - lr * buf
+ * with buf stored like FlashAdamW's m (MOMENTUM spec, or MOMENTUM_LINEAR with
+ * companded = 0, or fp32 with quantize_states = 0).  A zero buffer makes the
+ * first step buf = g, as torch's clone of the first gradient does.  Same
+ * parameter kinds and return values as fo_oracle_adamw_step. */
+int fo_oracle_sgd_step(int64_t n, void* param, int param_kind, void* rho, const void* grad, int grad_kind,
+                       void* m_state, uint16_t* m_scales, int quantize_states, int companded, double lr,
+                       double momentum, double weight_decay);
+
 #ifdef __cplusplus
 }
 #endif
