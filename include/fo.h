@@ -193,6 +193,24 @@ fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors,
                                 fo_state_format state_format, fo_dtype grad_dtype, double lr, double beta1,
                                 double beta2, double eps, double weight_decay, int64_t step, void* stream);
 
+/* ---- FlashSGD --------------------------------------------------------------
+ * The pages name FlashSGD only in the byte accounting of
+ * "code/flashsim/flash_adamw_sim.py" (`bytes_per_param`: theta' + rho and one
+ * quantized state, the momentum).  The update read here is SGD with momentum
+ * as torch.optim.SGD computes it (dampening 0, no Nesterov, weight decay added
+ * to the gradient), every operation rounded once:
+ *   g = fp32(grad); if weight_decay != 0: g = g + wd * theta;
+ *   buf = momentum * buf + g;  theta = theta - lr * buf
+ * lr, momentum, weight_decay are rounded once to fp32.  The buffer lives in
+ * fo_tensor_general.m / m_scales in the given state format (FO_STATE_COMPANDED
+ * = the MOMENTUM spec, FO_STATE_LINEAR = MOMENTUM_LINEAR, FO_STATE_F32 = fp32);
+ * v and v_scales are unused (may be NULL).  All-zero codes and scales are the
+ * initial buffer, so the first step stores buf = g as torch does.  Exact IEEE
+ * chain; same errors as fo_adamw_step_general. */
+fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
+                      fo_state_format state_format, fo_dtype grad_dtype, double lr, double momentum,
+                      double weight_decay, void* stream);
+
 /* Largest tensor list fo_adamw_step handles in a single kernel launch. */
 int fo_max_tensors_per_launch(void);
 

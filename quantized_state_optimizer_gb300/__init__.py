@@ -23,7 +23,7 @@ from .build import LIB as _LIB_PATH
 __all__ = [
     "FoError", "SPECS", "fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct",
     "fo_adamw_step", "fo_adamw_step_static", "FO_STATIC_MAX_TENSORS", "fo_adamw_step_general",
-    "FoTensorGeneral", "PARAM_FORMATS", "STATE_FORMATS", "fo_max_tensors_per_launch",
+    "FoTensorGeneral", "PARAM_FORMATS", "STATE_FORMATS", "fo_sgd_step", "fo_max_tensors_per_launch",
     "fo_device_status", "FoTensor", "lib", "lib_path",
 ]
 
@@ -100,12 +100,13 @@ def lib() -> ctypes.CDLL:
         L.fo_adamw_step_static.argtypes = [ctypes.POINTER(FoTensor), i32, i32, d, d, d, d, d, i64, i32, p]
         L.fo_adamw_step_general.argtypes = [ctypes.POINTER(FoTensorGeneral), i32, i32, i32, i32, d, d, d, d, d,
                                             i64, p]
+        L.fo_sgd_step.argtypes = [ctypes.POINTER(FoTensorGeneral), i32, i32, i32, i32, d, d, d, p]
         L.fo_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.fo_device_status.restype = i32
         L.fo_max_tensors_per_launch.argtypes = []
         L.fo_max_tensors_per_launch.restype = i32
         for f in ("fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct", "fo_adamw_step",
-                  "fo_adamw_step_static", "fo_adamw_step_general"):
+                  "fo_adamw_step_static", "fo_adamw_step_general", "fo_sgd_step"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -264,3 +265,21 @@ def fo_adamw_step_general(tensors, param_format, state_format, grad_dtype, lr: f
     _check("fo_adamw_step_general", lib().fo_adamw_step_general(
         arr, count, pf, sf, int(grad_dtype), float(lr), float(beta1), float(beta2), float(eps),
         float(weight_decay), int(step), _stream(stream)))
+
+
+def fo_sgd_step(tensors, param_format, state_format, grad_dtype, lr: float, momentum: float,
+                weight_decay: float, stream=None) -> None:
+    """One FlashSGD step over a list of ``FoTensorGeneral`` (the momentum buffer
+    in ``m`` / ``m_scales``; see include/fo.h for the update)."""
+    if isinstance(grad_dtype, torch.dtype):
+        grad_dtype = FO_DT_BF16 if grad_dtype == torch.bfloat16 else FO_DT_F32
+    pf = PARAM_FORMATS[param_format] if isinstance(param_format, str) else int(param_format)
+    sf = STATE_FORMATS[state_format] if isinstance(state_format, str) else int(state_format)
+    if isinstance(tensors, ctypes.Array):
+        arr, count = tensors, len(tensors)
+    else:
+        tensors = list(tensors)
+        count = len(tensors)
+        arr = (FoTensorGeneral * max(count, 1))(*tensors)
+    _check("fo_sgd_step", lib().fo_sgd_step(
+        arr, count, pf, sf, int(grad_dtype), float(lr), float(momentum), float(weight_decay), _stream(stream)))

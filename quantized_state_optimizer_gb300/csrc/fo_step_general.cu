@@ -27,6 +27,9 @@ constexpr int kGenTile = kThreads * kPerThread;
 
 struct GenArgs {
   StepScalars k;
+  int sgd;         // 0: AdamW (Algorithm 4); 1: SGD with momentum (fo_sgd_step)
+  float sgd_mu;    // SGD: momentum, and weight decay added to the gradient
+  float sgd_wd;
   int param_format;
   int state_format;
   int grad_bf16;
@@ -87,6 +90,23 @@ __global__ void __launch_bounds__(kThreads) general_step_kernel(const __grid_con
         default: theta[j] = static_cast<const float*>(T.param)[i]; break;
       }
       float mj, vj;
+      if (a.sgd) {
+        // SGD with momentum: the buffer is the m state; v is not used
+        if (a.state_format == FO_STATE_F32) {
+          mj = static_cast<const float*>(T.m)[i];
+        } else {
+          const int qm = static_cast<int>(static_cast<const int8_t*>(T.m)[i]);
+          const float sm = f16_bits_to_f32(T.m_scales[i / kGroup]);
+          mj = __fmul_rn(a.state_format == FO_STATE_COMPANDED ? code_unit_value<true, true>(qm)
+                                                              : code_unit_value<true, false>(qm),
+                         sm);
+        }
+        const float gd = a.decay ? __fadd_rn(g, __fmul_rn(a.sgd_wd, theta[j])) : g;
+        mj = __fadd_rn(__fmul_rn(a.sgd_mu, mj), gd);
+        theta[j] = __fsub_rn(theta[j], __fmul_rn(k.lr, mj));
+        m[j] = mj;
+        continue;
+      }
       if (a.state_format == FO_STATE_F32) {
         mj = static_cast<const float*>(T.m)[i];
         vj = static_cast<const float*>(T.v)[i];
@@ -119,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) general_step_kernel(const __grid_con
       for (int j = 0; j < kPerThread; ++j) {
         if (e0 + j >= n) continue;
         static_cast<float*>(T.m)[e0 + j] = m[j];
-        static_cast<float*>(T.v)[e0 + j] = v[j];
+        if (!a.sgd) static_cast<float*>(T.v)[e0 + j] = v[j];
       }
     } else {
       const bool companded = a.state_format == FO_STATE_COMPANDED;
@@ -142,11 +162,11 @@ __global__ void __launch_bounds__(kThreads) general_step_kernel(const __grid_con
         if (e0 + j >= n) continue;
         static_cast<int8_t*>(T.m)[e0 + j] = static_cast<int8_t>(
             companded ? encode_code<true, true>(m[j], dm) : encode_code<true, false>(m[j], dm));
-        static_cast<uint8_t*>(T.v)[e0 + j] = static_cast<uint8_t>(encode_code<false, false>(r[j], dv));
+        if (!a.sgd) static_cast<uint8_t*>(T.v)[e0 + j] = static_cast<uint8_t>(encode_code<false, false>(r[j], dv));
       }
       if (e0 < n && !(threadIdx.x & 1)) {
         T.m_scales[e0 / kGroup] = sm16;
-        T.v_scales[e0 / kGroup] = sv16;
+        if (!a.sgd) T.v_scales[e0 / kGroup] = sv16;
       }
     }
 
@@ -184,7 +204,7 @@ int rho_bytes(int f) { return f == FO_PARAM_BF16_RHO8 ? 1 : f == FO_PARAM_BF16_R
 int state_bytes(int f) { return f == FO_STATE_F32 ? 4 : 1; }
 
 // Writable buffers must not overlap anything; grads may overlap each other.
-bool general_overlap(const fo_tensor_general* ts, int n, int pf, int sf, int grad_bytes) {
+bool general_overlap(const fo_tensor_general* ts, int n, int pf, int sf, int grad_bytes, bool with_v) {
   struct Range {
     uintptr_t lo, hi;
     bool writable;
@@ -204,10 +224,10 @@ bool general_overlap(const fo_tensor_general* ts, int n, int pf, int sf, int gra
     if (rho_bytes(pf)) add(t.rho, rho_bytes(pf) * e, true);
     add(t.grad, grad_bytes * e, false);
     add(t.m, state_bytes(sf) * e, true);
-    add(t.v, state_bytes(sf) * e, true);
+    if (with_v) add(t.v, state_bytes(sf) * e, true);
     if (sf != FO_STATE_F32) {
       add(t.m_scales, 2 * g, true);
-      add(t.v_scales, 2 * g, true);
+      if (with_v) add(t.v_scales, 2 * g, true);
     }
   }
   std::sort(r.begin(), r.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
@@ -226,41 +246,40 @@ bool general_overlap(const fo_tensor_general* ts, int n, int pf, int sf, int gra
 
 using namespace fo;
 
-extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
-                                           fo_state_format state_format, fo_dtype grad_dtype, double lr, double beta1,
-                                           double beta2, double eps, double weight_decay, int64_t step, void* stream) {
+namespace fo {
+namespace {
+
+// Checks shared by both entry points; `with_v` is false for SGD (one state).
+fo_status check_general(const fo_tensor_general* tensors, int n_tensors, int param_format, int state_format,
+                        int grad_dtype, bool with_v) {
   if (n_tensors < 0 || (n_tensors > 0 && !tensors)) return FO_ERR_INVALID_ARG;
   if (param_format < FO_PARAM_BF16_RHO8 || param_format > FO_PARAM_F32) return FO_ERR_INVALID_ARG;
   if (state_format < FO_STATE_COMPANDED || state_format > FO_STATE_F32) return FO_ERR_INVALID_ARG;
   if (grad_dtype != FO_DT_F32 && grad_dtype != FO_DT_BF16) return FO_ERR_INVALID_ARG;
-  if (step < 1) return FO_ERR_INVALID_ARG;
-  if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
-  if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return FO_ERR_INVALID_ARG;
   const bool quantized = state_format != FO_STATE_F32;
   const bool has_rho = param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16;
   for (int i = 0; i < n_tensors; ++i) {
     const fo_tensor_general& t = tensors[i];
     if (t.numel < 0) return FO_ERR_INVALID_ARG;
     if (t.numel == 0) continue;
-    if (!t.param || !t.grad || !t.m || !t.v || (has_rho && !t.rho) || (quantized && (!t.m_scales || !t.v_scales)))
+    if (!t.param || !t.grad || !t.m || (with_v && !t.v) || (has_rho && !t.rho) ||
+        (quantized && (!t.m_scales || (with_v && !t.v_scales))))
       return FO_ERR_INVALID_ARG;
-    if (!aligned16(t.param) || !aligned16(t.grad) || !aligned16(t.m) || !aligned16(t.v) ||
-        (has_rho && !aligned16(t.rho)) || (quantized && (!aligned16(t.m_scales) || !aligned16(t.v_scales))))
+    if (!aligned16(t.param) || !aligned16(t.grad) || !aligned16(t.m) || (with_v && !aligned16(t.v)) ||
+        (has_rho && !aligned16(t.rho)) ||
+        (quantized && (!aligned16(t.m_scales) || (with_v && !aligned16(t.v_scales)))))
       return FO_ERR_MISALIGNED;
   }
-  const int grad_bytes = grad_dtype == FO_DT_BF16 ? 2 : 4;
-  if (general_overlap(tensors, n_tensors, param_format, state_format, grad_bytes)) return FO_ERR_ALIAS;
+  if (general_overlap(tensors, n_tensors, param_format, state_format, grad_dtype == FO_DT_BF16 ? 2 : 4, with_v))
+    return FO_ERR_ALIAS;
+  return FO_OK;
+}
 
-  GenArgs args;
-  args.k = step_scalars(lr, beta1, beta2, eps, weight_decay, step);
-  args.param_format = param_format;
-  args.state_format = state_format;
-  args.grad_bf16 = grad_dtype == FO_DT_BF16;
-  args.decay = weight_decay != 0.0;
-  cudaStream_t s = as_stream(stream);
+// Launches over the list, 400 tensors per launch; `args` carries the scalars
+// and formats.
+fo_status launch_general(const fo_tensor_general* tensors, int n_tensors, GenArgs& args, cudaStream_t s) {
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-
   int i = 0;
   while (i < n_tensors) {
     int cnt = 0;
@@ -282,4 +301,44 @@ extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int
     if (st != FO_OK) return st;
   }
   return FO_OK;
+}
+
+}  // namespace
+}  // namespace fo
+
+extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
+                                           fo_state_format state_format, fo_dtype grad_dtype, double lr, double beta1,
+                                           double beta2, double eps, double weight_decay, int64_t step, void* stream) {
+  fo_status st = check_general(tensors, n_tensors, param_format, state_format, grad_dtype, true);
+  if (st != FO_OK) return st;
+  if (step < 1) return FO_ERR_INVALID_ARG;
+  if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
+  if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return FO_ERR_INVALID_ARG;
+  GenArgs args;
+  args.k = step_scalars(lr, beta1, beta2, eps, weight_decay, step);
+  args.sgd = 0;
+  args.sgd_mu = args.sgd_wd = 0.0f;
+  args.param_format = param_format;
+  args.state_format = state_format;
+  args.grad_bf16 = grad_dtype == FO_DT_BF16;
+  args.decay = weight_decay != 0.0;
+  return launch_general(tensors, n_tensors, args, as_stream(stream));
+}
+
+extern "C" fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
+                                 fo_state_format state_format, fo_dtype grad_dtype, double lr, double momentum,
+                                 double weight_decay, void* stream) {
+  fo_status st = check_general(tensors, n_tensors, param_format, state_format, grad_dtype, false);
+  if (st != FO_OK) return st;
+  if (!std::isfinite(lr) || !std::isfinite(momentum) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
+  GenArgs args;
+  args.k = step_scalars(lr, 0.0, 0.0, 1.0, 0.0, 1);  // only k.lr is used: RN(lr)
+  args.sgd = 1;
+  args.sgd_mu = static_cast<float>(momentum);
+  args.sgd_wd = static_cast<float>(weight_decay);
+  args.param_format = param_format;
+  args.state_format = state_format;
+  args.grad_bf16 = grad_dtype == FO_DT_BF16;
+  args.decay = weight_decay != 0.0;
+  return launch_general(tensors, n_tensors, args, as_stream(stream));
 }

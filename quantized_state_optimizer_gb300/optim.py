@@ -15,7 +15,7 @@ from __future__ import annotations
 
 import torch
 
-from . import FoTensor, fo_adamw_step, fo_split, n_groups
+from . import FoTensor, FoTensorGeneral, fo_adamw_step, fo_sgd_step, fo_split, n_groups
 
 _ALIGN_BYTES = 16
 
@@ -278,3 +278,46 @@ class FlashAdamW(torch.optim.Optimizer):
         for (t, gdt), items in by_key.items():
             fo_adamw_step([ft for ft, _ in items], gdt, group["lr"], beta1, beta2, group["eps"],
                           group["weight_decay"], t, self.rho_bits)
+
+
+class FlashSGD(torch.optim.Optimizer):
+    """SGD with momentum on bf16 parameters with a split master weight and an
+    8-bit group-quantized momentum buffer (``fo_sgd_step``; the update rule is
+    the reading stated in include/fo.h).  ``master_weight_bits`` = 24 (int8 rho)
+    or 32 (int16 rho).  One launch per (param group, grad dtype)."""
+
+    def __init__(self, params, lr=1e-2, momentum=0.9, weight_decay=0.0, master_weight_bits: int = 24):
+        if master_weight_bits not in (24, 32):
+            raise ValueError("master_weight_bits must be 24 or 32")
+        super().__init__(params, dict(lr=lr, momentum=momentum, weight_decay=weight_decay))
+        self.rho_bits = 8 if master_weight_bits == 24 else 16
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        pf = "bf16_rho8" if self.rho_bits == 8 else "bf16_rho16"
+        for group in self.param_groups:
+            by_dtype: dict[torch.dtype, list] = {}
+            for p in group["params"]:
+                if p.grad is None:
+                    continue
+                if p.dtype != torch.bfloat16 or not p.is_cuda or not p.is_contiguous():
+                    raise TypeError("FlashSGD parameters must be contiguous bf16 CUDA tensors")
+                st = self.state[p]
+                if len(st) == 0:
+                    n = p.numel()
+                    st["rho"] = torch.zeros(n, dtype=torch.int8 if self.rho_bits == 8 else torch.int16,
+                                            device=p.device)
+                    st["m_codes"] = torch.zeros(n, dtype=torch.int8, device=p.device)
+                    st["m_scales"] = torch.zeros(n_groups(n), dtype=torch.float16, device=p.device)
+                g = p.grad if p.grad.is_contiguous() else p.grad.contiguous()
+                ft = FoTensorGeneral(p.data_ptr(), st["rho"].data_ptr(), g.data_ptr(), st["m_codes"].data_ptr(),
+                                     st["m_scales"].data_ptr(), None, None, p.numel())
+                by_dtype.setdefault(g.dtype, []).append((ft, g))
+            for gdt, items in by_dtype.items():
+                fo_sgd_step([ft for ft, _ in items], pf, "companded", gdt, group["lr"], group["momentum"],
+                            group["weight_decay"])
+        return loss

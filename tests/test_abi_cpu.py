@@ -148,3 +148,13 @@ def test_general_step_host_checks(L):
     assert call(0, 2) == INVALID          # a split needs rho
     assert call(3, 0) == INVALID          # quantized states need scales
     assert L.fo_adamw_step_general(None, 0, 3, 2, 1, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None) == OK
+
+
+def test_sgd_step_host_checks(L):
+    """fo_sgd_step needs no v buffers, and rejects bad arguments before any CUDA call."""
+    t = fo.FoTensorGeneral(1 << 32, 0, (1 << 32) + (2 << 20), (1 << 32) + (3 << 20), 0, 0, 0, 1000)
+    arr = (fo.FoTensorGeneral * 1)(t)
+    assert L.fo_sgd_step(arr, 1, 3, 0, 1, 1e-2, 0.9, 0.0, None) == INVALID   # quantized buffer needs scales
+    assert L.fo_sgd_step(arr, 1, 4, 2, 1, 1e-2, 0.9, 0.0, None) == INVALID   # no such parameter format
+    assert L.fo_sgd_step(arr, 1, 3, 2, 1, float("nan"), 0.9, 0.0, None) == INVALID
+    assert L.fo_sgd_step(None, 0, 3, 2, 1, 1e-2, 0.9, 0.0, None) == OK
