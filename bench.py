@@ -166,14 +166,14 @@ def bench_specs(layers: int | None):
     return [s for s in specs if s.name.startswith(keep)]
 
 
-def build_state(device, layers: int | None = None, fmt: str | None = None):
+def build_state(device, layers: int | None = None, fmt: str | None = None, optimizer: str = "adamw"):
     from quantized_state_optimizer_gb300.optim import FlashAdamWState
     all_specs = W.llama_tensor_list(MODEL)
     specs = bench_specs(layers)
     numels = [s.numel for s in specs]
     wid = W.WORKLOAD_IDS[MODEL.name]
     if fmt is not None:
-        st = GeneralState(numels, *fmt.split(":"), device)
+        st = GeneralState(numels, *fmt.split(":"), device, optimizer)
     else:
         st = FlashAdamWState(numels, rho_bits=RHO_BITS, grad_dtype=torch.bfloat16, device=device)
     for i, s in enumerate(specs):
@@ -185,21 +185,22 @@ def build_state(device, layers: int | None = None, fmt: str | None = None):
 
 
 # ------------------------------------------------- the ablation formats
-def general_bytes_per_param(pf: str, sf: str) -> float:
-    """Algorithmic bytes of one step per parameter in a format (bf16 grads)."""
+def general_bytes_per_param(pf: str, sf: str, optimizer: str = "adamw") -> float:
+    """Algorithmic bytes of one step per parameter in a format (bf16 grads):
+    AdamW reads and writes two states, SGD one (the momentum)."""
     param = 4 if pf == "f32" else 2
     rho = {"bf16_rho8": 1, "bf16_rho16": 2}.get(pf, 0)
-    states = 16.0 if sf == "f32" else 4.0 + 4 * 2 / 32
-    return 2 + 2 * param + 2 * rho + states
+    one_state = 8.0 if sf == "f32" else 2.0 + 2 * 2 / 32
+    return 2 + 2 * param + 2 * rho + (2 if optimizer == "adamw" else 1) * one_state
 
 
 class GeneralState:
     """Flat device slabs of the list in one of the ablation formats, and the
     ``fo_tensor_general`` array over them (for ``fo_adamw_step_general``)."""
 
-    def __init__(self, numels, pf: str, sf: str, device):
+    def __init__(self, numels, pf: str, sf: str, device, optimizer: str = "adamw"):
         import quantized_state_optimizer_gb300 as fo
-        self.pf, self.sf = pf, sf
+        self.pf, self.sf, self.optimizer = pf, sf, optimizer
         align = lambda n: (n + 15) // 16 * 16  # noqa: E731
         offs, o = [], 0
         for n in numels:
@@ -242,8 +243,11 @@ class GeneralState:
 
     def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
         import quantized_state_optimizer_gb300 as fo
-        fo.fo_adamw_step_general(self.arr, self.pf, self.sf, torch.bfloat16, lr, beta1, beta2, eps,
-                                 weight_decay, t, stream)
+        if self.optimizer == "sgd":  # momentum beta1, the same lr and weight decay
+            fo.fo_sgd_step(self.arr, self.pf, self.sf, torch.bfloat16, lr, beta1, weight_decay, stream)
+        else:
+            fo.fo_adamw_step_general(self.arr, self.pf, self.sf, torch.bfloat16, lr, beta1, beta2, eps,
+                                     weight_decay, t, stream)
 
 
 def time_steps(st, steps: int, warmup: int, stream, dist_on: bool) -> tuple[float, list[float]]:
@@ -439,6 +443,9 @@ def main():
                     help="profiling only: restrict to the first N decoder layers' tensors")
     ap.add_argument("--host-link", action="store_true",
                     help="only measure pinned host <-> device copy bandwidth and print it as JSON")
+    ap.add_argument("--optimizer", default="adamw", choices=["adamw", "sgd"],
+                    help="sgd: time FlashSGD (fo_sgd_step, momentum = beta1) in --format "
+                         "(default bf16_rho8:companded)")
     ap.add_argument("--format", default=None,
                     help="PARAM:STATES, e.g. bf16:linear or f32:f32 -- time fo_adamw_step_general in an "
                          "ablation format (parameter: bf16_rho8, bf16_rho16, bf16, f32; states: companded, "
@@ -481,7 +488,9 @@ def main():
     import quantized_state_optimizer_gb300 as fo
     fo.lib()  # fail loudly if the CUDA library is missing
 
-    st, numels = build_state(device, args.layers, args.format)
+    if args.optimizer == "sgd" and args.format is None:
+        args.format = "bf16_rho8:companded"
+    st, numels = build_state(device, args.layers, args.format, args.optimizer)
     stream = torch.cuda.Stream(device=device)
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(st, args.steps, args.warmup, stream, dist_on)
@@ -489,7 +498,7 @@ def main():
     n = sum(numels)
     value = job_throughput(n, ws, ms)
     bytes_step = (algorithmic_bytes(numels) if args.format is None
-                  else int(round(general_bytes_per_param(*args.format.split(":")) * sum(numels))))
+                  else int(round(general_bytes_per_param(*args.format.split(":"), args.optimizer) * sum(numels))))
     kernel_ms = statistics.mean(per)
     peak, peak_kind = load_peak()
     achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
@@ -511,7 +520,8 @@ def main():
     if args.layers is not None:
         cfg["workload"] = f"PROFILING SUBSET (first {args.layers} layers) of " + cfg["workload"]
     if args.format is not None:
-        cfg["workload"] = (f"ABLATION FORMAT {args.format} (fo_adamw_step_general, exact chain) of the "
+        entry = "fo_sgd_step, FlashSGD, momentum 0.9" if args.optimizer == "sgd" else "fo_adamw_step_general"
+        cfg["workload"] = (f"FORMAT {args.format} ({entry}, exact chain) of the "
                            f"{MODEL.name} list: {len(numels)} tensors, {sum(numels):,} params, bf16 grads")
     cfg["bytes_per_step"] = bytes_step
     cfg["bytes_per_param"] = bytes_step / n
