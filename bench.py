@@ -66,26 +66,35 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
 # 1.554265 GB read + 1.062396 GB written for 218,112,000 parameters.  Traffic
 # grows with the parameters processed, so a full launch is that figure times
 # the list's size.  It stands only for the kernel sources it was taken on.
+# DRAM bytes per parameter of the pipelined kernels, from one ncu capture
+# each (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the
+# 218,112,000 parameters of decoder layer 0, bf16 grads, int8 rho), keyed by
+# (kernel, format) and valid only for the kernel sources they were taken on.
+_CAPTURE_SOURCES = {
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "30ca2bfe32bdb6ecb548a68a36a2277bc944c948660707a548e6b821e068b779",
+    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
+}
 TRAFFIC_CAPTURE = {
-    "bytes_per_param": (1.554265e9 + 1.062396e9) / 218112000,
-    "sha256": {
-        "quantized_state_optimizer_gb300/csrc/fo_step.cu": "af6e7a328bc49b2fa33ca220ffe02c902560e529b54144a5555b675b3db29c01",
-        "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
-    },
+    ("fo::adamw_step_kernel", None): (1.554250496e9 + 1.061571584e9) / 218112000,
+    ("fo::sgd_step_kernel", "bf16_rho8:companded"): (1.322522880e9 + 0.829238272e9) / 218112000,
 }
 
 
-def captured_traffic(n_params: int) -> float | None:
-    """Per-launch DRAM traffic scaled from the capture, or None once the kernel changed."""
+def captured_traffic(n_params: int, kernel: str = "fo::adamw_step_kernel", fmt: str | None = None) -> float | None:
+    """Per-launch DRAM traffic scaled from the capture, or None when there is
+    no capture for this kernel and format or the kernel changed since."""
     import hashlib
-    for rel, digest in TRAFFIC_CAPTURE["sha256"].items():
+    per_param = TRAFFIC_CAPTURE.get((kernel, fmt))
+    if per_param is None:
+        return None
+    for rel, digest in _CAPTURE_SOURCES.items():
         try:
             with open(os.path.join(ROOT, rel), "rb") as fh:
                 if hashlib.sha256(fh.read()).hexdigest() != digest:
                     return None
         except OSError:
             return None
-    return TRAFFIC_CAPTURE["bytes_per_param"] * n_params
+    return per_param * n_params
 
 
 def load_peak() -> tuple[float, str]:
@@ -192,6 +201,18 @@ def general_bytes_per_param(pf: str, sf: str, optimizer: str = "adamw") -> float
     rho = {"bf16_rho8": 1, "bf16_rho16": 2}.get(pf, 0)
     one_state = 8.0 if sf == "f32" else 2.0 + 2 * 2 / 32
     return 2 + 2 * param + 2 * rho + (2 if optimizer == "adamw" else 1) * one_state
+
+
+def step_kernel_name(fmt: str | None, optimizer: str) -> str:
+    """The kernel one step launches: the pipelined kernel for the paper's
+    format (AdamW, or SGD with companded codes and a split master), else the
+    general kernel."""
+    if fmt is None:
+        return "fo::adamw_step_kernel"
+    pf, sf = fmt.split(":")
+    if optimizer == "sgd" and sf == "companded" and pf in ("bf16_rho8", "bf16_rho16"):
+        return "fo::sgd_step_kernel"
+    return "fo::general_step_kernel"
 
 
 class GeneralState:
@@ -521,7 +542,7 @@ def main():
         cfg["workload"] = f"PROFILING SUBSET (first {args.layers} layers) of " + cfg["workload"]
     if args.format is not None:
         entry = "fo_sgd_step, FlashSGD, momentum 0.9" if args.optimizer == "sgd" else "fo_adamw_step_general"
-        cfg["workload"] = (f"FORMAT {args.format} ({entry}, exact chain) of the "
+        cfg["workload"] = (f"FORMAT {args.format} ({entry}, {step_kernel_name(args.format, args.optimizer)}) of the "
                            f"{MODEL.name} list: {len(numels)} tensors, {sum(numels):,} params, bf16 grads")
     cfg["bytes_per_step"] = bytes_step
     cfg["bytes_per_param"] = bytes_step / n
@@ -533,9 +554,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
                      "frac_of_nominal_8000_gbs": achieved / 8000.0,
-                     "kernel": "fo::adamw_step_kernel" if args.format is None else "fo::general_step_kernel",
+                     "kernel": step_kernel_name(args.format, args.optimizer),
                      "kernel_ms": kernel_ms, "bytes_per_launch": bytes_step,
-                     "traffic": captured_traffic(n) if args.layers is None and args.format is None else None},
+                     "traffic": (captured_traffic(n, step_kernel_name(args.format, args.optimizer), args.format)
+                                 if args.layers is None else None)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,

@@ -205,8 +205,13 @@ fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors,
  * fo_tensor_general.m / m_scales in the given state format (FO_STATE_COMPANDED
  * = the MOMENTUM spec, FO_STATE_LINEAR = MOMENTUM_LINEAR, FO_STATE_F32 = fp32);
  * v and v_scales are unused (may be NULL).  All-zero codes and scales are the
- * initial buffer, so the first step stores buf = g as torch does.  Exact IEEE
- * chain; same errors as fo_adamw_step_general. */
+ * initial buffer, so the first step stores buf = g as torch does.
+ * In the paper's format (FO_PARAM_BF16_RHO8 or FO_PARAM_BF16_RHO16 with
+ * FO_STATE_COMPANDED) the step runs in the pipelined kernel of fo_adamw_step,
+ * one HBM pass, momentum codes certified from a hardware reciprocal with the
+ * exact chain as fallback (the same bits); other formats run the exact IEEE
+ * chain.  Same errors as fo_adamw_step_general; the pipelined kernel also
+ * reports a bounded wait that ran out through fo_device_status(). */
 fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
                       fo_state_format state_format, fo_dtype grad_dtype, double lr, double momentum,
                       double weight_decay, void* stream);

@@ -331,6 +331,10 @@ extern "C" fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors
   fo_status st = check_general(tensors, n_tensors, param_format, state_format, grad_dtype, false);
   if (st != FO_OK) return st;
   if (!std::isfinite(lr) || !std::isfinite(momentum) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
+  if (state_format == FO_STATE_COMPANDED &&
+      (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
+    return launch_sgd_fast(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
+                           lr, momentum, weight_decay, as_stream(stream));
   GenArgs args;
   args.k = step_scalars(lr, 0.0, 0.0, 1.0, 0.0, 1);  // only k.lr is used: RN(lr)
   args.sgd = 1;
