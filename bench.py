@@ -314,17 +314,18 @@ def time_e2e(st, numels, steps: int, stream) -> dict:
     t = 1000
     st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param, stream=stream)
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for k in range(steps):
         t += 1
         st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param, stream=stream)
-    t1.record(stream)
+        ev[k + 1].record(stream)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    ms = ev[0].elapsed_time(ev[steps]) / steps
     n = sum(numels)
     return {"value": n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "ms_per_step_min": min(per), "ms_per_step_max": max(per),
             "h2d_bytes_per_step": int(host_grad.numel() * host_grad.element_size()),
             "d2h_bytes_per_step": int(host_param.numel() * host_param.element_size()),
             "steps": steps, "api": "FlashAdamWState.step_from_host (8 chunks, copies overlapped)"}
@@ -455,7 +456,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-sample", type=int, default=436_224_000,
                     help="parameters of the CPU-oracle sample (default: two decoder layers, ~10 s of work)")
     ap.add_argument("--cpu-steps", type=int, default=20)
@@ -525,6 +526,12 @@ def main():
     achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
     try:
         e2e = time_e2e(st, numels, args.e2e_steps, stream) if args.e2e_steps > 0 and args.format is None else None
+        if e2e is not None:
+            # the link's own ceiling on this machine, for reading the e2e number
+            link = host_link(gib=2)
+            moved = e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"]
+            e2e["link_both_directions_gbs"] = link["both_directions_gbs"]
+            e2e["link_floor_ms"] = moved / 1e9 / link["both_directions_gbs"] * 1e3
     except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
         e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
     del st
