@@ -425,6 +425,65 @@ def host_link(gib: int = 8) -> dict:
             "both_directions_gbs": 2 * gb / timed(both), "bytes_each": int(n * 2)}
 
 
+# --------------------------------------------------- standalone kernels
+def pair_kernels(n: int = 1 << 30, reps: int = 5) -> dict:
+    """The standalone kernels on ``n`` fp32 elements (far above L2): fo_quantize
+    and fo_dequantize in all four specs, fo_split and fo_reconstruct for both
+    rho widths.  Per kernel: the mean launch time over ``reps`` launches (CUDA
+    events on the launching stream, after two warm-up launches) and its
+    algorithmic bytes per launch against the measured copy bandwidth."""
+    import quantized_state_optimizer_gb300 as fo
+    peak, src = load_peak()
+    dev = torch.device("cuda")
+    ng = (n + 31) // 32
+    gen = torch.Generator(device=dev).manual_seed(5)
+    x = torch.randn(n, device=dev, generator=gen) * 1e-3
+    out = torch.empty(n, device=dev)
+    codes = {True: torch.empty(n, dtype=torch.int8, device=dev), False: torch.empty(n, dtype=torch.uint8, device=dev)}
+    scales = torch.empty(ng, dtype=torch.float16, device=dev)
+    theta_bf = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    rhos = {8: torch.empty(n, dtype=torch.int8, device=dev), 16: torch.empty(n, dtype=torch.int16, device=dev)}
+    stream = torch.cuda.Stream()
+
+    def timed(fn) -> float:
+        with torch.cuda.stream(stream):  # torch ops too run on the timed stream
+            for _ in range(2):
+                fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    rows = []
+
+    def add(kernel, variant, ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append({"kernel": kernel, "variant": variant, "ms": ms, "bytes": nbytes, "gbs": gbs,
+                     "frac": gbs / peak})
+
+    for spec in ("momentum", "variance", "momentum_linear", "variance_linear"):
+        signed = spec.startswith("momentum")
+        src_x = x if signed else x.abs()  # the variance specs take values >= 0
+        c = codes[signed]
+        add("fo_quantize", spec, timed(lambda: fo.fo_quantize(src_x, spec, c, scales, stream)), 5 * n + 2 * ng)
+        add("fo_dequantize", spec, timed(lambda: fo.fo_dequantize(c, scales, spec, out, stream)), 5 * n + 2 * ng)
+    # a library copy with dequantize's traffic (1 B read, 4 B written per
+    # element): the write-heavy ceiling that kernel is measured against
+    add("torch copy int8 -> fp32", "same bytes as fo_dequantize", timed(lambda: out.copy_(codes[True])), 5 * n)
+    for rb in (8, 16):
+        r = rhos[rb]
+        nb = 4 * n + 2 * n + rb // 8 * n
+        add("fo_split", f"rho{rb}", timed(lambda: fo.fo_split(x, rb, theta_bf, r, stream)), nb)
+        add("fo_reconstruct", f"rho{rb}", timed(lambda: fo.fo_reconstruct(theta_bf, r, rb, out, stream)), nb)
+    return {"pair_kernels": rows, "n": n, "peak_gbs": peak, "peak_source": src, "reps": reps,
+            "timing": "CUDA events on the launching stream; inputs far larger than L2"}
+
+
 # ------------------------------------------------------------ main
 def max_over_ranks(ms: float, device) -> float:
     """The slowest rank's step time: every rank must have finished a step for
@@ -465,6 +524,9 @@ def main():
                     help="profiling only: restrict to the first N decoder layers' tensors")
     ap.add_argument("--host-link", action="store_true",
                     help="only measure pinned host <-> device copy bandwidth and print it as JSON")
+    ap.add_argument("--pairs", action="store_true",
+                    help="time the standalone kernels (fo_quantize / fo_dequantize / fo_split / "
+                         "fo_reconstruct) on 2^30 elements and print their achieved GB/s")
     ap.add_argument("--optimizer", default="adamw", choices=["adamw", "sgd"],
                     help="sgd: time FlashSGD (fo_sgd_step, momentum = beta1) in --format "
                          "(default bf16_rho8:companded)")
@@ -500,6 +562,9 @@ def main():
 
     if args.host_link:
         print(json.dumps({"host_link": host_link()}), flush=True)
+        return
+    if args.pairs:
+        print(json.dumps(pair_kernels()), flush=True)
         return
 
     dist_on = ws > 1

@@ -7,6 +7,8 @@
 // 128-bit loads and stores, a group of 32 shared by two neighbouring lanes.
 #include <string>
 
+#include <algorithm>
+
 #include "fo.h"
 #include "fo_device.cuh"
 #include "fo_host.h"
@@ -41,40 +43,44 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) r[j] = (e0 + j < n) ? x[e0 + j] : 0.0f;
   }
-  if (kSqrt) {
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) r[j] = __fsqrt_rn(r[j]);
-  }
+  // Group maximum of |x| (signed specs) or x.  With the square root, the
+  // group's value is RN(sqrt(max x)): a correctly rounded square root is
+  // monotone, so that is the maximum of RN(sqrt(x)) over the group.
   float a = kSigned ? fabsf(r[0]) : r[0];
 #pragma unroll
   for (int j = 1; j < kPerThread; ++j) a = keep_first_max(a, kSigned ? fabsf(r[j]) : r[j]);
   a = group_max_pair(a);
+  if (kSqrt) a = __fsqrt_rn(a);
   const uint16_t s16 = f32_to_f16_bits(a);
   const float safe = guarded_divisor(s16);
 
+  // Certified approximate codes, exact where uncertain.  The code argument t
+  // (127 softsign(x/s), 127 x/s, 255 sqrt(x)/s or 255 x/s) comes from group
+  // constants and at most one hardware approximation; its error is far below
+  // the margin that round_code_certified leaves around every half-integer.
   V16B out;
-  if constexpr (kSigned == kSoftsign) {
-    // momentum (softsign) and both unsigned specs (r c2 = 255 r/s whether or
-    // not r is a square root): certified approximate codes, exact where uncertain
+  {
     const float rs = __fdiv_rn(1.0f, safe);
     const float c1 = __fmul_rn(254.0f, rs);
     const float c2 = __fdiv_rn(255.0f, safe);
+    const float c127 = __fdiv_rn(127.0f, safe);
     uint32_t near = 0;
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
       bool nj;
-      const float t = kSigned ? momentum_t_approx(r[j], rs, c1) : variance_t_approx_from_root(r[j], c2);
+      float t;
+      if (kSigned && kSoftsign) t = momentum_t_approx(r[j], rs, c1);
+      else if (kSigned) t = fminf(fmaxf(__fmul_rn(r[j], c127), -127.0f), 127.0f);
+      else t = variance_t_approx_from_root(kSqrt ? sqrt_approx(r[j]) : r[j], c2);
       out.u8[j] = round_code_certified(t, nj);
       if (nj) near |= 1u << j;
     }
     if (near) {
 #pragma unroll
       for (int j = 0; j < kPerThread; ++j)
-        if (near & (1u << j)) out.u8[j] = static_cast<uint8_t>(encode_code<kSigned, kSoftsign>(r[j], safe));
+        if (near & (1u << j))
+          out.u8[j] = static_cast<uint8_t>(encode_code<kSigned, kSoftsign>(kSqrt ? __fsqrt_rn(r[j]) : r[j], safe));
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) out.u8[j] = static_cast<uint8_t>(encode_code<kSigned, kSoftsign>(r[j], safe));
   }
   uint8_t* c = static_cast<uint8_t*>(codes);
   if (e0 + kPerThread <= n) {
@@ -92,38 +98,46 @@ template <bool kSigned, bool kSqrt, bool kSoftsign>
 __global__ void __launch_bounds__(kThreads)
     dequantize_kernel(const void* __restrict__ codes, const uint16_t* __restrict__ scales,
                       int64_t n, float* __restrict__ out) {
-  const int64_t e0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * kPerThread;
-  if (e0 >= n) return;
+  // unit value of every code byte, with the element-wise definition's operations
+  __shared__ float lut[256];
+  static_assert(kThreads == 256, "one table entry per thread");
+  lut[threadIdx.x] = code_unit_value<kSigned, kSoftsign>(kSigned ? static_cast<int>(static_cast<int8_t>(threadIdx.x))
+                                                                 : static_cast<int>(threadIdx.x));
+  __syncthreads();
+  // grid-stride over chunks of kThreads * kPerThread elements (the table is
+  // built once per block)
   const uint8_t* c = static_cast<const uint8_t*>(codes);
-  V16B w;
-  const bool full = e0 + kPerThread <= n;
-  if (full) {
-    w.q = ld_stream(c + e0);
-  } else {
+  for (int64_t e0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * kPerThread; e0 < n;
+       e0 += static_cast<int64_t>(gridDim.x) * kThreads * kPerThread) {
+    V16B w;
+    const bool full = e0 + kPerThread <= n;
+    if (full) {
+      w.q = ld_stream(c + e0);
+    } else {
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) w.u8[j] = (e0 + j < n) ? c[e0 + j] : 0;
-  }
-  const float s = f16_bits_to_f32(scales[e0 / kGroup]);
-  float o[kPerThread];
-#pragma unroll
-  for (int j = 0; j < kPerThread; ++j) {
-    const int q = kSigned ? static_cast<int>(w.i8[j]) : static_cast<int>(w.u8[j]);
-    float y = __fmul_rn(code_unit_value<kSigned, kSoftsign>(q), s);
-    if (kSqrt) y = __fmul_rn(y, y);
-    o[j] = y;
-  }
-  if (full) {
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      V16B t;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) t.f32[k] = o[4 * v + k];
-      st_stream(out + e0 + 4 * v, t.q);
+      for (int j = 0; j < kPerThread; ++j) w.u8[j] = (e0 + j < n) ? c[e0 + j] : 0;
     }
-  } else {
+    const float s = f16_bits_to_f32(scales[e0 / kGroup]);
+    float o[kPerThread];
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j)
-      if (e0 + j < n) out[e0 + j] = o[j];
+    for (int j = 0; j < kPerThread; ++j) {
+      float y = __fmul_rn(lut[w.u8[j]], s);
+      if (kSqrt) y = __fmul_rn(y, y);
+      o[j] = y;
+    }
+    if (full) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        V16B t;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t.f32[k] = o[4 * v + k];
+        st_stream(out + e0 + 4 * v, t.q);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPerThread; ++j)
+        if (e0 + j < n) out[e0 + j] = o[j];
+    }
   }
 }
 
@@ -273,7 +287,9 @@ fo_status fo_dequantize(const void* codes, const uint16_t* scales, int64_t n, fo
   if (n == 0) return FO_OK;
   if (!codes || !scales || !out) return FO_ERR_INVALID_ARG;
   if (!aligned16(codes) || !aligned16(scales) || !aligned16(out)) return FO_ERR_MISALIGNED;
-  const unsigned grid = blocks_for(n);
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned grid = std::min<unsigned>(blocks_for(n), static_cast<unsigned>(sms) * 8);  // 8 blocks per SM
   cudaStream_t s = as_stream(stream);
   switch (spec) {
     case FO_SPEC_MOMENTUM: dequantize_kernel<true, false, true><<<grid, kThreads, 0, s>>>(codes, scales, n, out); break;

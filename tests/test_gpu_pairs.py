@@ -57,8 +57,8 @@ def test_quantize_battery_bit_exact(spec):
 def test_quantize_ragged_sizes(n):
     rng = np.random.default_rng(n)
     x = (rng.standard_normal(n) * np.exp(2 * rng.standard_normal(n))).astype(np.float32)
-    for spec in ("momentum", "variance"):
-        xin = np.abs(x) if spec == "variance" else x
+    for spec in SPECS:
+        xin = np.abs(x) if spec.startswith("variance") else x
         c, s, d = gpu_quantize(xin, spec)
         rc, rs = O.quantize(xin, spec)
         assert np.array_equal(c, rc) and np.array_equal(s, rs), (n, spec)
@@ -71,13 +71,17 @@ def _boundary_inputs(spec: str) -> np.ndarray:
     is exactly k + 1/2 (round-half-even territory): every one of them must
     take the exact path and still agree with the oracle."""
     out = []
-    ks = np.arange(0, 127) if spec == "momentum" else np.arange(0, 255)
+    ks = np.arange(0, 127) if spec.startswith("momentum") else np.arange(0, 255)
     for k in ks:
         if spec == "momentum":
             z = (k + 0.5) / 127.0
             x0 = z / (2.0 - z)            # inverse softsign at scale 1
-        else:
+        elif spec == "variance":
             x0 = ((k + 0.5) / 255.0) ** 2  # inverse of 255 sqrt(v)
+        elif spec == "momentum_linear":
+            x0 = (k + 0.5) / 127.0
+        else:
+            x0 = (k + 0.5) / 255.0
         x0 = np.float32(x0)
         nb = [np.float32(np.nextafter(x0, np.float32(np.inf * d))) for d in (1, -1)]
         cand = [x0, nb[0], nb[1], np.float32(np.nextafter(nb[0], np.float32(np.inf))),
@@ -85,19 +89,42 @@ def _boundary_inputs(spec: str) -> np.ndarray:
         g = np.zeros(32, np.float32)
         g[0] = 1.0
         g[1:1 + len(cand)] = cand
-        if spec == "momentum":
+        if spec.startswith("momentum"):
             g[8:8 + len(cand)] = [-c for c in cand]
         out.append(g)
     return np.concatenate(out)
 
 
-@pytest.mark.parametrize("spec", ["momentum", "variance"])
+@pytest.mark.parametrize("spec", SPECS)
 def test_quantize_half_code_boundaries(spec):
     x = _boundary_inputs(spec)
     c, s, d = gpu_quantize(x, spec)
     rc, rs = O.quantize(x, spec)
     assert np.array_equal(s, rs)
     assert np.array_equal(c, rc), np.flatnonzero(c != rc)[:10]
+
+
+@pytest.mark.parametrize("spec", SPECS)
+def test_quantize_volume_heavy_tailed(spec):
+    """4M values over many orders of magnitude, with zeros, subnormals and
+    groups whose maximum is tiny or huge: the certified codes and their exact
+    fallback against the oracle, and the dequantized values."""
+    rng = np.random.default_rng(11)
+    n = (1 << 22) + 9
+    x = (rng.standard_normal(n) * np.exp(4 * rng.standard_normal(n))).astype(np.float32)
+    x[::97] = 0.0
+    x[5::101] = np.float32(3e-39)
+    x[7::4099] *= np.float32(1e30)
+    x[11::8191] = np.float32(2e-30)
+    x = np.clip(x, -3e38, 3e38).astype(np.float32)
+    if spec.startswith("variance"):
+        x = np.abs(x)
+    x = np.concatenate([x, _boundary_inputs(spec)])
+    c, s, d = gpu_quantize(x, spec)
+    rc, rs = O.quantize(x, spec)
+    assert np.array_equal(s, rs), spec
+    assert np.array_equal(c, rc), (spec, np.flatnonzero(c != rc)[:10])
+    assert same_f32(d, O.dequantize(rc, rs, spec)), spec
 
 
 def test_quantize_does_not_write_past_n():
