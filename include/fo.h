@@ -164,9 +164,11 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
  *                                   plain group-32 absmax codes of m and of v
  *              FO_STATE_F32         fp32 m and v, no scales (quantize_states
  *                                   False)
- * Every result is the exact binary32 definition (the kernel evaluates the IEEE
- * chain, with no approximation).  fo_adamw_step is the fast path for the two
- * FO_PARAM_BF16_RHO* formats with FO_STATE_COMPANDED and gives the same bits.
+ * Every result is the exact binary32 definition: codes and the 24-bit master
+ * come from certified approximations with the exact chain as fallback (the
+ * same bits), all else from the IEEE chain itself.  fo_adamw_step is the fast
+ * path for the two FO_PARAM_BF16_RHO* formats with FO_STATE_COMPANDED and
+ * gives the same bits.
  * Buffers as in fo_tensor, with widths by format: param 2 or 4 bytes per
  * element, rho 1 or 2 (unused, may be NULL, without a split), m and v 1 byte
  * (codes) or 4 (fp32), m_scales / v_scales fp16 [ceil(numel/32)] (unused, may
@@ -209,8 +211,8 @@ fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors,
  * In the paper's format (FO_PARAM_BF16_RHO8 or FO_PARAM_BF16_RHO16 with
  * FO_STATE_COMPANDED) the step runs in the pipelined kernel of fo_adamw_step,
  * one HBM pass, momentum codes certified from a hardware reciprocal with the
- * exact chain as fallback (the same bits); other formats run the exact IEEE
- * chain.  Same errors as fo_adamw_step_general; the pipelined kernel also
+ * exact chain as fallback (the same bits); other formats run the kernel of
+ * fo_adamw_step_general.  Same errors as fo_adamw_step_general; the pipelined kernel also
  * reports a bounded wait that ran out through fo_device_status(). */
 fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
                       fo_state_format state_format, fo_dtype grad_dtype, double lr, double momentum,
