@@ -71,12 +71,12 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
 # 218,112,000 parameters of decoder layer 0, bf16 grads, int8 rho), keyed by
 # (kernel, format) and valid only for the kernel sources they were taken on.
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "30ca2bfe32bdb6ecb548a68a36a2277bc944c948660707a548e6b821e068b779",
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "0993c9d2e126e2b834a24311b643f0fbc8735f2aec71fbeb6b7a03ef9dcbcbc2",
     "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
 }
 TRAFFIC_CAPTURE = {
-    ("fo::adamw_step_kernel", None): (1.554250496e9 + 1.061571584e9) / 218112000,
-    ("fo::sgd_step_kernel", "bf16_rho8:companded"): (1.322522880e9 + 0.829238272e9) / 218112000,
+    ("fo::adamw_step_kernel", None): (1.554716416e9 + 1.061582592e9) / 218112000,
+    ("fo::sgd_step_kernel", "bf16_rho8:companded"): (1.322390528e9 + 0.829249536e9) / 218112000,
 }
 
 
@@ -204,14 +204,17 @@ def general_bytes_per_param(pf: str, sf: str, optimizer: str = "adamw") -> float
 
 
 def step_kernel_name(fmt: str | None, optimizer: str) -> str:
-    """The kernel one step launches: the pipelined kernel for the paper's
-    format (AdamW, or SGD with companded codes and a split master), else the
-    general kernel."""
+    """The kernel one step launches: the pipelined kernel for a split master
+    with codes (AdamW's companded format through fo_adamw_step, its linear one
+    through fo_adamw_step_general; SGD with either), else the general kernel."""
     if fmt is None:
         return "fo::adamw_step_kernel"
     pf, sf = fmt.split(":")
-    if optimizer == "sgd" and sf == "companded" and pf in ("bf16_rho8", "bf16_rho16"):
+    split = pf in ("bf16_rho8", "bf16_rho16")
+    if optimizer == "sgd" and split and sf in ("companded", "linear"):
         return "fo::sgd_step_kernel"
+    if optimizer == "adamw" and split and sf == "linear":
+        return "fo::adamw_step_kernel"
     return "fo::general_step_kernel"
 
 

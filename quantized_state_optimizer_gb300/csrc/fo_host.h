@@ -36,10 +36,17 @@ struct StepScalars {
 };
 StepScalars step_scalars(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
 
-// SGD with momentum in the paper's format (bf16 theta' with int8 or int16
-// rho, companded momentum codes) through the pipelined step kernel; the list
-// must already have passed the checks of fo_sgd_step.
-fo_status launch_sgd_fast(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits, double lr,
-                          double momentum, double weight_decay, cudaStream_t s);
+// SGD with momentum with a split master (bf16 theta' with int8 or int16 rho)
+// and companded or linear momentum codes, through the pipelined step kernel;
+// the list must already have passed the checks of fo_sgd_step.
+fo_status launch_sgd_fast(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits, bool companded,
+                          double lr, double momentum, double weight_decay, cudaStream_t s);
+
+// AdamW with linear codes and a split master through the pipelined step
+// kernel; the list must already have passed the checks of
+// fo_adamw_step_general.
+fo_status launch_adamw_linear(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits,
+                              double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step,
+                              cudaStream_t s);
 
 }  // namespace fo

@@ -488,6 +488,11 @@ extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int
   if (step < 1) return FO_ERR_INVALID_ARG;
   if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
   if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return FO_ERR_INVALID_ARG;
+  // linear codes with a split master: the pipelined kernel (the companded
+  // ones stay here, where they cross-check fo_adamw_step)
+  if (state_format == FO_STATE_LINEAR && (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
+    return launch_adamw_linear(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
+                               lr, beta1, beta2, eps, weight_decay, step, as_stream(stream));
   GenArgs args;
   args.k = step_scalars(lr, beta1, beta2, eps, weight_decay, step);
   args.sgd = 0;
@@ -506,10 +511,9 @@ extern "C" fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors
   fo_status st = check_general(tensors, n_tensors, param_format, state_format, grad_dtype, false);
   if (st != FO_OK) return st;
   if (!std::isfinite(lr) || !std::isfinite(momentum) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
-  if (state_format == FO_STATE_COMPANDED &&
-      (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
+  if (state_format != FO_STATE_F32 && (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
     return launch_sgd_fast(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
-                           lr, momentum, weight_decay, as_stream(stream));
+                           state_format == FO_STATE_COMPANDED, lr, momentum, weight_decay, as_stream(stream));
   GenArgs args;
   args.k = step_scalars(lr, 0.0, 0.0, 1.0, 0.0, 1);  // only k.lr is used: RN(lr)
   args.sgd = 1;

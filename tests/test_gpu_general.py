@@ -156,3 +156,41 @@ def test_general_kernel_equals_fast_kernel_in_the_papers_format(rho_bits):
             for a, b in ((v["param"], d.param), (v["rho"], d.rho), (v["m_codes"], d.m), (v["v_codes"], d.v),
                          (v["m_scales"], d.ms), (v["v_scales"], d.vs)):
                 assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (i, t)
+
+
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("pf", ["bf16_rho8", "bf16_rho16"])
+def test_linear_codes_split_master_pipelined(pf, grad_dtype):
+    """Linear codes with a split master run in the pipelined kernel: several
+    full tiles of each width (7680, 6656 and 6144 elements), ragged tails and
+    heavy-tailed weights and gradients, against the oracle bit for bit."""
+    h = W.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.05, steps=3)
+    numels = [70000, 7680 * 3, 31, 6656 * 2 + 3, 6144 * 2, (1 << 20) + 5]
+
+    def theta_of(i, n):
+        g = torch.Generator().manual_seed(800 + i)
+        return (torch.randn(n, generator=g) * torch.exp(torch.randn(n, generator=g) * 2) * 0.02).float()
+
+    thetas = [theta_of(i, n) for i, n in enumerate(numels)]
+    dev = [DevTensor(t, pf, "linear", grad_dtype) for t in thetas]
+    refs = [_oracle_state(t, pf, "linear") for t in thetas]
+    arr = (FoTensorGeneral * len(dev))(*[d.ft() for d in dev])
+    for t in range(1, h.steps + 1):
+        for i, n in enumerate(numels):
+            g = torch.Generator().manual_seed(W.grad_seed(57, i, t))
+            # tails up to about 1e2: v stays inside fp16's range, so every
+            # linear v scale is finite (an infinite one makes the next step's
+            # states NaN, outside the step's preconditions)
+            x = torch.randn(n, generator=g) * torch.exp(torch.randn(n, generator=g) * 2) * 1e-3
+            x = x if grad_dtype == torch.float32 else x.to(torch.bfloat16)
+            dev[i].grad.copy_(x.to(DEV))
+            gn = x.numpy() if grad_dtype == torch.float32 else x.view(torch.int16).numpy().view(np.uint16)
+            O.adamw_step(refs[i], gn, t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, companded=False)
+        fo.fo_adamw_step_general(arr, pf, "linear", grad_dtype, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, t)
+        torch.cuda.synchronize()
+        for i in range(len(numels)):
+            got, r = dev[i].host(), refs[i]
+            ctx = (pf, str(grad_dtype), i, t)
+            for key, ref in (("param", r.param), ("rho", r.rho), ("m", r.m), ("v", r.v), ("ms", r.m_scales),
+                             ("vs", r.v_scales)):
+                _same(got[key], ref, ctx + (key,))

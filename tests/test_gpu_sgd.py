@@ -89,10 +89,10 @@ def test_flash_sgd_optimizer_matches_oracle():
 # elements (bf16 grads, int8 rho), 6656 (bf16, int16 rho; fp32, int8 rho) or
 # 6144 (fp32, int16 rho).
 
-def _run_sgd(numels, pf, grad_dtype, lr, mu, wd, steps, grad_fn=None, theta_fn=None):
+def _run_sgd(numels, pf, grad_dtype, lr, mu, wd, steps, grad_fn=None, theta_fn=None, sf="companded"):
     thetas = [theta_fn(i, n) if theta_fn else _theta(i, n) for i, n in enumerate(numels)]
-    dev = [DevTensor(t, pf, "companded", grad_dtype) for t in thetas]
-    refs = [_oracle_state(t, pf, "companded") for t in thetas]
+    dev = [DevTensor(t, pf, sf, grad_dtype) for t in thetas]
+    refs = [_oracle_state(t, pf, sf) for t in thetas]
     arr = (FoTensorGeneral * len(dev))(*[d.ft() for d in dev])
     for k in range(len(arr)):
         arr[k].v = None
@@ -105,8 +105,8 @@ def _run_sgd(numels, pf, grad_dtype, lr, mu, wd, steps, grad_fn=None, theta_fn=N
             g = g if grad_dtype == torch.float32 else g.to(torch.bfloat16)
             dev[i].grad.copy_(g.to(DEV))
             gn = g.numpy() if grad_dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16)
-            O.sgd_step(refs[i], gn, lr, mu, wd)
-        fo.fo_sgd_step(arr, pf, "companded", grad_dtype, lr, mu, wd)
+            O.sgd_step(refs[i], gn, lr, mu, wd, companded=sf == "companded")
+        fo.fo_sgd_step(arr, pf, sf, grad_dtype, lr, mu, wd)
         torch.cuda.synchronize()
         for i, n in enumerate(numels):
             if n == 0:
@@ -119,12 +119,13 @@ def _run_sgd(numels, pf, grad_dtype, lr, mu, wd, steps, grad_fn=None, theta_fn=N
             _same(got["ms"], r.m_scales, ctx + ("m_scales",))
 
 
+@pytest.mark.parametrize("sf", ["companded", "linear"])
 @pytest.mark.parametrize("mu,wd", [(0.9, 0.01), (0.9, 0.0), (0.0, 0.0)])
 @pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("pf", ["bf16_rho8", "bf16_rho16"])
-def test_sgd_fast_kernel_full_tiles(pf, grad_dtype, mu, wd):
+def test_sgd_fast_kernel_full_tiles(pf, grad_dtype, mu, wd, sf):
     numels = [70000, 7680 * 3, 31, 6656 * 2 + 3, 0, 6144 * 2, 100003]
-    _run_sgd(numels, pf, grad_dtype, 1e-2, mu, wd, 3)
+    _run_sgd(numels, pf, grad_dtype, 1e-2, mu, wd, 3, sf=sf)
 
 
 def test_sgd_more_tensors_than_one_launch():
@@ -133,8 +134,9 @@ def test_sgd_more_tensors_than_one_launch():
     _run_sgd(numels, "bf16_rho8", torch.bfloat16, 1e-2, 0.9, 0.01, 2)
 
 
+@pytest.mark.parametrize("sf", ["companded", "linear"])
 @pytest.mark.parametrize("pf", ["bf16_rho8", "bf16_rho16"])
-def test_sgd_volume_heavy_tailed(pf):
+def test_sgd_volume_heavy_tailed(pf, sf):
     """Millions of elements, weights and gradients over many orders of magnitude."""
     def theta_fn(i, n):
         g = torch.Generator().manual_seed(700 + i)
@@ -144,7 +146,7 @@ def test_sgd_volume_heavy_tailed(pf):
         g = torch.Generator().manual_seed(W.grad_seed(88, i, t))
         return torch.randn(n, generator=g) * torch.exp(torch.randn(n, generator=g) * 3) * 1e-3
 
-    _run_sgd([(1 << 22) + 5, 3 * (1 << 20)], pf, torch.bfloat16, 1e-2, 0.9, 0.05, 4, grad_fn, theta_fn)
+    _run_sgd([(1 << 22) + 5, 3 * (1 << 20)], pf, torch.bfloat16, 1e-2, 0.9, 0.05, 4, grad_fn, theta_fn, sf=sf)
 
 
 def test_sgd_half_integer_codes_overflow_the_redo_queue():
