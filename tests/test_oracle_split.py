@@ -47,9 +47,9 @@ def test_master32_round_trip_exhaustive():
         x = bits.view(np.float32)
         hi, rho = O.split(x, 32)
         back = O.reconstruct(hi, rho, 32).view(np.uint32)
-        nan = np.isnan(x)
-        assert np.array_equal(back[~nan], bits[~nan]), hex(start)
-        assert np.all(np.isnan(back[nan].view(np.float32)))
+        bad = np.flatnonzero(back != bits)  # only NaN patterns may come back changed
+        assert np.all(np.isnan(x[bad])), (hex(start), bad[:5])
+        assert np.all(np.isnan(back[bad].view(np.float32))), hex(start)
 
 
 @pytest.mark.slow
