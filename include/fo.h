@@ -168,7 +168,9 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
  * come from certified approximations with the exact chain as fallback (the
  * same bits), all else from the IEEE chain itself.  fo_adamw_step is the fast
  * path for the two FO_PARAM_BF16_RHO* formats with FO_STATE_COMPANDED and
- * gives the same bits.
+ * gives the same bits; with FO_STATE_LINEAR those two formats run in the same
+ * pipelined kernel (linear-code instantiation), which reports a bounded wait
+ * that ran out through fo_device_status().
  * Buffers as in fo_tensor, with widths by format: param 2 or 4 bytes per
  * element, rho 1 or 2 (unused, may be NULL, without a split), m and v 1 byte
  * (codes) or 4 (fp32), m_scales / v_scales fp16 [ceil(numel/32)] (unused, may
