@@ -36,7 +36,7 @@ struct GenArgs {
   int state_format;
   int grad_bf16;
   int decay;
-  int fast_theta;  // AdamW with the 24-bit master and eps >= 2^-40: certified theta
+  int fast_theta;  // AdamW with the 24-bit master or a bf16 parameter, eps >= 2^-40: certified theta
   int n_tensors;
   int64_t total_tiles;
   int64_t tile_start[kGenMaxTensors + 1];
@@ -221,6 +221,15 @@ __global__ void __launch_bounds__(kThreads, kGenMinBlocks<PF>) general_step_kern
           const uint32_t wl = __float_as_uint(__fsub_rn(th, __fadd_rn(dl, e))) + 0x8080u;
           const uint32_t wh = __float_as_uint(__fsub_rn(th, __fsub_rn(dl, e))) + 0x8080u;
           w24[j] = (wl ^ wh) > 0xFFu ? split_word<8>(__fsub_rn(th, general_delta(mj, vj, k))) : wl;
+        } else if (PF == FO_PARAM_BF16 && a.fast_theta) {
+          // bf16 parameter: the same interval, rounded to nearest even bf16
+          // (monotone too); one bf16 for both ends is the exact result's
+          const float den = __fadd_rn(__fmul_rn(sqrt_approx(vj), k.sqrt_ib2), k.eps);
+          const float dl = __fmul_rn(__fmul_rn(mj, k.lr_ib1), rcp_approx(den));
+          const float e = __fmaf_rn(fabsf(dl), kGenDeltaRel, kGenDeltaAbs);
+          const uint16_t bl = f32_to_bf16_rne(__fsub_rn(th, __fadd_rn(dl, e)));
+          const uint16_t bh = f32_to_bf16_rne(__fsub_rn(th, __fsub_rn(dl, e)));
+          th = bl == bh ? __uint_as_float(static_cast<uint32_t>(bl) << 16) : __fsub_rn(th, general_delta(mj, vj, k));
         } else {
           th = __fsub_rn(th, general_delta(mj, vj, k));
           if (PF == FO_PARAM_BF16_RHO8) w24[j] = split_word<8>(th);
@@ -501,7 +510,7 @@ extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int
   args.state_format = state_format;
   args.grad_bf16 = grad_dtype == FO_DT_BF16;
   args.decay = weight_decay != 0.0;
-  args.fast_theta = param_format == FO_PARAM_BF16_RHO8 && args.k.eps >= 0x1p-40f;
+  args.fast_theta = (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16) && args.k.eps >= 0x1p-40f;
   return launch_general(tensors, n_tensors, args, as_stream(stream));
 }
 
