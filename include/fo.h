@@ -164,9 +164,10 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
  *                                   plain group-32 absmax codes of m and of v
  *              FO_STATE_F32         fp32 m and v, no scales (quantize_states
  *                                   False)
- * Every result is the exact binary32 definition: codes and the 24-bit master
- * come from certified approximations with the exact chain as fallback (the
- * same bits), all else from the IEEE chain itself.  fo_adamw_step is the fast
+ * Every result is the exact binary32 definition: codes, the 24-bit master and
+ * a bf16 parameter without a split come from certified approximations with
+ * the exact chain as fallback (the same bits), all else from the IEEE chain
+ * itself.  fo_adamw_step is the fast
  * path for the two FO_PARAM_BF16_RHO* formats with FO_STATE_COMPANDED and
  * gives the same bits; with FO_STATE_LINEAR those two formats run in the same
  * pipelined kernel (linear-code instantiation), which reports a bounded wait

@@ -3,9 +3,10 @@
 // `master_weight_bits` in {24, 32, None}, an fp32 parameter, `companded` and
 // `quantize_states`): the ablations the paper compares the method against.
 //
-// Every result equals the exact IEEE chain of the definition.  Codes and the
-// 24-bit master come from certified approximations with an in-thread exact
-// fallback, as in the fused kernel; everything else is computed exactly.  The
+// Every result equals the exact IEEE chain of the definition.  Codes, the
+// 24-bit master and a bf16 parameter without a split come from certified
+// approximations with an in-thread exact fallback, as in the fused kernel;
+// everything else is computed exactly.  The
 // paper's own format runs in the fused kernel of fo_step.cu; this one serves
 // the ablation formats.  One launch covers a list of tensors, with one kernel
 // instantiation per format; a block takes a tile of 4096 elements, a thread
