@@ -203,6 +203,24 @@ def general_bytes_per_param(pf: str, sf: str, optimizer: str = "adamw") -> float
     return 2 + 2 * param + 2 * rho + (2 if optimizer == "adamw" else 1) * one_state
 
 
+class PerTensorSteps:
+    """The step as gradient release issues it: one single-tensor
+    ``fo_adamw_step`` launch per tensor (what ``FlashAdamW(gradient_release=
+    True)`` launches from each parameter's post-accumulate-grad hook), here
+    back to back on one stream."""
+
+    def __init__(self, st):
+        from quantized_state_optimizer_gb300 import FoTensor
+        full = st.fo_tensors()
+        self.st = st
+        self.arrs = [(FoTensor * 1)(full[i]) for i in range(len(st.numels))]
+
+    def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
+        from quantized_state_optimizer_gb300 import fo_adamw_step
+        for arr in self.arrs:
+            fo_adamw_step(arr, self.st.grad_dtype, lr, beta1, beta2, eps, weight_decay, t, self.st.rho_bits, stream)
+
+
 def step_kernel_name(fmt: str | None, optimizer: str) -> str:
     """The kernel one step launches: the pipelined kernel for a split master
     with codes (AdamW's companded format through fo_adamw_step, its linear one
@@ -527,6 +545,8 @@ def main():
                     help="profiling only: restrict to the first N decoder layers' tensors")
     ap.add_argument("--host-link", action="store_true",
                     help="only measure pinned host <-> device copy bandwidth and print it as JSON")
+    ap.add_argument("--per-tensor", action="store_true",
+                    help="time the step as gradient release launches it: one single-tensor launch per tensor")
     ap.add_argument("--pairs", action="store_true",
                     help="time the standalone kernels (fo_quantize / fo_dequantize / fo_split / "
                          "fo_reconstruct) on 2^30 elements and print their achieved GB/s")
@@ -582,8 +602,9 @@ def main():
         args.format = "bf16_rho8:companded"
     st, numels = build_state(device, args.layers, args.format, args.optimizer)
     stream = torch.cuda.Stream(device=device)
+    stepper = PerTensorSteps(st) if args.per_tensor else st
     with ClockSampler(local) as clk:
-        total_ms, per = time_steps(st, args.steps, args.warmup, stream, dist_on)
+        total_ms, per = time_steps(stepper, args.steps, args.warmup, stream, dist_on)
     ms = max_over_ranks(total_ms / args.steps, device)
     n = sum(numels)
     value = job_throughput(n, ws, ms)
@@ -593,7 +614,8 @@ def main():
     peak, peak_kind = load_peak()
     achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
     try:
-        e2e = time_e2e(st, numels, args.e2e_steps, stream) if args.e2e_steps > 0 and args.format is None else None
+        e2e = (time_e2e(st, numels, args.e2e_steps, stream)
+               if args.e2e_steps > 0 and args.format is None and not args.per_tensor else None)
         if e2e is not None:
             # the link's own ceiling on this machine, for reading the e2e number
             link = host_link(gib=2)
@@ -602,7 +624,7 @@ def main():
             e2e["link_floor_ms"] = moved / 1e9 / link["both_directions_gbs"] * 1e3
     except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
         e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
-    del st
+    del st, stepper
     torch.cuda.empty_cache()
 
     if rank != 0:
@@ -619,6 +641,9 @@ def main():
         entry = "fo_sgd_step, FlashSGD, momentum 0.9" if args.optimizer == "sgd" else "fo_adamw_step_general"
         cfg["workload"] = (f"FORMAT {args.format} ({entry}, {step_kernel_name(args.format, args.optimizer)}) of the "
                            f"{MODEL.name} list: {len(numels)} tensors, {sum(numels):,} params, bf16 grads")
+    if args.per_tensor:
+        cfg["workload"] = (f"PER-TENSOR LAUNCHES (the gradient-release step: {len(numels)} single-tensor "
+                           f"fo_adamw_step launches per step, back to back) of " + cfg["workload"])
     cfg["bytes_per_step"] = bytes_step
     cfg["bytes_per_param"] = bytes_step / n
     cfg["hbm_gbs"] = achieved
@@ -632,10 +657,10 @@ def main():
                      "kernel": step_kernel_name(args.format, args.optimizer),
                      "kernel_ms": kernel_ms, "bytes_per_launch": bytes_step,
                      "traffic": (captured_traffic(n, step_kernel_name(args.format, args.optimizer), args.format)
-                                 if args.layers is None else None)},
+                                 if args.layers is None and not args.per_tensor else None)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (len(numels) if args.per_tensor else 1),
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
