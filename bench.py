@@ -71,12 +71,12 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
 # 218,112,000 parameters of decoder layer 0, bf16 grads, int8 rho), keyed by
 # (kernel, format) and valid only for the kernel sources they were taken on.
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "0993c9d2e126e2b834a24311b643f0fbc8735f2aec71fbeb6b7a03ef9dcbcbc2",
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "54adec4c2e88071d273693cc91ffa708fb20c673dec6a62525daaad05a81019f",
     "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
 }
 TRAFFIC_CAPTURE = {
-    ("fo::adamw_step_kernel", None): (1.554716416e9 + 1.061582592e9) / 218112000,
-    ("fo::sgd_step_kernel", "bf16_rho8:companded"): (1.322390528e9 + 0.829249536e9) / 218112000,
+    ("fo::adamw_step_kernel", None): (1.554244096e9 + 1.061031680e9) / 218112000,
+    ("fo::sgd_step_kernel", "bf16_rho8:companded"): (1.322391296e9 + 0.828948992e9) / 218112000,
 }
 
 

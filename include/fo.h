@@ -233,6 +233,15 @@ int fo_max_tensors_per_launch(void);
 #define FO_DEVICE_WAIT_TIMEOUT 1u
 fo_status fo_device_status(uint32_t* status);
 
+/* Failure detection without a fault (no counterpart on the pages).  Launches
+ * one block that waits, with the step kernel's bounded mbarrier wait, on a
+ * barrier that nothing completes; after `polls` unsuccessful polls (1 ..
+ * 2^22, the step kernel's own limit) it gives up and sets bit 0 of the device
+ * status word, as the step kernel does when one of its waits runs out.  The
+ * context stays usable.  FO_ERR_INVALID_ARG for polls out of range; a launch
+ * failure gives FO_ERR_CUDA. */
+fo_status fo_check_wait_timeout(uint32_t polls, void* stream);
+
 /* ---- allocation-free step -------------------------------------------------
  * No counterpart on the pages: an interface of this library.  Same arguments,
  * results and errors as fo_adamw_step, for a list of at most

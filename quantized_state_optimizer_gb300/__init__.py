@@ -24,7 +24,7 @@ __all__ = [
     "FoError", "SPECS", "fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct",
     "fo_adamw_step", "fo_adamw_step_static", "FO_STATIC_MAX_TENSORS", "fo_adamw_step_general",
     "FoTensorGeneral", "PARAM_FORMATS", "STATE_FORMATS", "fo_sgd_step", "fo_max_tensors_per_launch",
-    "fo_device_status", "FoTensor", "lib", "lib_path",
+    "fo_device_status", "fo_check_wait_timeout", "FoTensor", "lib", "lib_path",
 ]
 
 SPECS = {"momentum": 0, "variance": 1, "momentum_linear": 2, "variance_linear": 3}
@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
         L.fo_sgd_step.argtypes = [ctypes.POINTER(FoTensorGeneral), i32, i32, i32, i32, d, d, d, p]
         L.fo_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.fo_device_status.restype = i32
+        L.fo_check_wait_timeout.argtypes = [ctypes.c_uint32, p]
+        L.fo_check_wait_timeout.restype = i32
         L.fo_max_tensors_per_launch.argtypes = []
         L.fo_max_tensors_per_launch.restype = i32
         for f in ("fo_quantize", "fo_dequantize", "fo_split", "fo_reconstruct", "fo_adamw_step",
@@ -193,6 +195,13 @@ def fo_reconstruct(theta_bf16: torch.Tensor, rho: torch.Tensor, rho_bits: int, t
 # ------------------------------------------------------------------ step
 def fo_max_tensors_per_launch() -> int:
     return lib().fo_max_tensors_per_launch()
+
+
+def fo_check_wait_timeout(polls: int = 4096, stream=None) -> None:
+    """One block whose bounded wait on a barrier that nothing completes runs out
+    after ``polls`` polls and sets the timeout bit that ``fo_device_status``
+    reports (failure detection, exercised without a fault)."""
+    _check("fo_check_wait_timeout", lib().fo_check_wait_timeout(ctypes.c_uint32(int(polls)), _stream(stream)))
 
 
 def fo_device_status() -> int:

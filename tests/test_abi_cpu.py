@@ -64,6 +64,11 @@ def test_pair_argument_errors(L):
     assert L.fo_reconstruct(FAKE, FAKE, 0, 16, None, None) == OK
 
 
+def test_wait_timeout_probe_rejects_bad_poll_counts(L):
+    assert L.fo_check_wait_timeout(0, None) == INVALID
+    assert L.fo_check_wait_timeout((1 << 22) + 1, None) == INVALID
+
+
 def _t(base, n, grad=None, stride=1 << 20):
     return fo.FoTensor(base, base + stride, grad if grad is not None else base + 2 * stride,
                        base + 3 * stride, base + 4 * stride, base + 5 * stride, base + 6 * stride, n)

@@ -357,3 +357,20 @@ def test_gradient_release_matches_step():
             for k in ("rho", "m_codes", "m_scales", "v_codes", "v_scales"):
                 assert torch.equal(sa[k].view(torch.uint8), sb[k].view(torch.uint8)), (k, t)
     opt_b.remove_hooks()
+
+
+def test_bounded_wait_running_out_is_reported():
+    """Failure detection without a fault: a wait that nothing completes gives
+    up after its poll limit, the timeout bit reaches the host through
+    fo_device_status (which clears it), and the context stays usable."""
+    fo.fo_device_status()  # clear anything left by earlier tests
+    for polls in (1, 4096):
+        fo.fo_check_wait_timeout(polls)
+        torch.cuda.synchronize()
+        assert fo.fo_device_status() == 1, polls
+        assert fo.fo_device_status() == 0
+    # the same process goes on stepping bit-exactly
+    run_small([4096 + 17, 100], 8, torch.bfloat16, W.LLAMA3_8B_HYPER, 2)
+    assert fo.fo_device_status() == 0
+    with pytest.raises(fo.FoError):
+        fo.fo_check_wait_timeout(0)
