@@ -624,6 +624,7 @@ def main():
             e2e["link_floor_ms"] = moved / 1e9 / link["both_directions_gbs"] * 1e3
     except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
         e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
+    footprint = st.bytes_allocated() if hasattr(st, "bytes_allocated") else None
     del st, stepper
     torch.cuda.empty_cache()
 
@@ -644,6 +645,13 @@ def main():
     if args.per_tensor:
         cfg["workload"] = (f"PER-TENSOR LAUNCHES (the gradient-release step: {len(numels)} single-tensor "
                            f"fo_adamw_step launches per step, back to back) of " + cfg["workload"])
+    if footprint is not None:
+        # the state's HBM footprint between steps (grads included) against the
+        # paper's storage accounting for this format
+        from quantized_state_optimizer_gb300.accounting import storage_bytes_per_param
+        cfg["state_bytes_per_param"] = footprint / n
+        cfg["state_bytes_per_param_accounted"] = storage_bytes_per_param(
+            "bf16_rho8" if RHO_BITS == 8 else "bf16_rho16", "companded")["total"]
     cfg["bytes_per_step"] = bytes_step
     cfg["bytes_per_param"] = bytes_step / n
     cfg["hbm_gbs"] = achieved

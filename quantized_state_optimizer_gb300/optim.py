@@ -87,6 +87,13 @@ class FlashAdamWState:
     def total_numel(self) -> int:
         return sum(self.numels)
 
+    def bytes_allocated(self) -> int:
+        """Device bytes of every slab (the state's HBM footprint, padding included)."""
+        slabs = [self.param, self.rho, self.m_codes, self.v_codes, self.m_scales, self.v_scales]
+        if self.grad is not None:
+            slabs.append(self.grad)
+        return sum(t.numel() * t.element_size() for t in slabs)
+
     # ------------------------------------------------------------ set-up
     def init_theta(self, i: int, theta: torch.Tensor, stream=None) -> None:
         """Split an fp32 master weight into this tensor's theta' and rho."""
