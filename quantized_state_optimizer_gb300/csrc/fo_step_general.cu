@@ -66,6 +66,18 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) { return __bfloat16
 constexpr float kGenDeltaRel = 0x1p-19f;
 constexpr float kGenDeltaAbs = 0x1p-100f;
 
+// Rare exact fallbacks kept out of line, so that the unrolled element loop
+// stays small enough for the instruction cache (measured: the bf16-parameter
+// and code formats gain 3-12 %; the 24-bit master's fallback stays inline,
+// where a call made the fp32-state format 9 % slower).
+__device__ __noinline__ float exact_theta(float theta, float m, float v, StepScalars k) {
+  return __fsub_rn(theta, general_delta(m, v, k));
+}
+template <bool kSigned, bool kSoftsign>
+__device__ __noinline__ uint32_t exact_code(float r, float divisor) {
+  return static_cast<uint8_t>(encode_code<kSigned, kSoftsign>(r, divisor));
+}
+
 // Inputs of one element as values: gradient, master weight, old m and v.
 struct GenIn {
   float g, theta, m, v;
@@ -230,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, kGenMinBlocks<PF>) general_step_kern
           const float e = __fmaf_rn(fabsf(dl), kGenDeltaRel, kGenDeltaAbs);
           const uint16_t bl = f32_to_bf16_rne(__fsub_rn(th, __fadd_rn(dl, e)));
           const uint16_t bh = f32_to_bf16_rne(__fsub_rn(th, __fsub_rn(dl, e)));
-          th = bl == bh ? __uint_as_float(static_cast<uint32_t>(bl) << 16) : __fsub_rn(th, general_delta(mj, vj, k));
+          th = bl == bh ? __uint_as_float(static_cast<uint32_t>(bl) << 16) : exact_theta(th, mj, vj, k);
         } else {
           th = __fsub_rn(th, general_delta(mj, vj, k));
           if (PF == FO_PARAM_BF16_RHO8) w24[j] = split_word<8>(th);
@@ -288,12 +300,12 @@ __global__ void __launch_bounds__(kThreads, kGenMinBlocks<PF>) general_step_kern
         bool near;
         const float tm = kComp ? momentum_t_approx(m[j], rs, c1) : fminf(fmaxf(__fmul_rn(m[j], c127), -127.0f), 127.0f);
         uint32_t cm = round_code_certified(tm, near);
-        if (near) cm = static_cast<uint8_t>(kComp ? encode_code<true, true>(m[j], dm) : encode_code<true, false>(m[j], dm));
+        if (near) cm = kComp ? exact_code<true, true>(m[j], dm) : exact_code<true, false>(m[j], dm);
         cmw[j >> 2] |= cm << (8 * (j & 3));
         if (!SGD) {
           const float tv = variance_t_approx_from_root(kComp ? sqrt_approx(v[j]) : v[j], c2);
           uint32_t cv = round_code_certified(tv, near);
-          if (near) cv = static_cast<uint8_t>(encode_code<false, false>(kComp ? __fsqrt_rn(v[j]) : v[j], dv));
+          if (near) cv = exact_code<false, false>(kComp ? __fsqrt_rn(v[j]) : v[j], dv);
           cvw[j >> 2] |= cv << (8 * (j & 3));
         }
       }
