@@ -346,7 +346,7 @@ def time_e2e(st, numels, steps: int, stream) -> dict:
     ms = ev[0].elapsed_time(ev[steps]) / steps
     n = sum(numels)
     return {"value": n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
-            "ms_per_step_min": min(per), "ms_per_step_max": max(per),
+            "ms_per_step_min": min(per), "ms_per_step_median": statistics.median(per), "ms_per_step_max": max(per),
             "h2d_bytes_per_step": int(host_grad.numel() * host_grad.element_size()),
             "d2h_bytes_per_step": int(host_param.numel() * host_param.element_size()),
             "steps": steps, "api": "FlashAdamWState.step_from_host (8 chunks, copies overlapped)"}
