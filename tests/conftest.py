@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    """Skip gpu-marked tests when no GPU is present (they are run with -m gpu on a GPU machine)."""
+    """Skip gpu-marked tests when no GPU is present (run them with -m gpu on a machine with one)."""
     try:
         import torch
         has_gpu = torch.cuda.is_available()
