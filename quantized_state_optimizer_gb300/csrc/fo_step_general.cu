@@ -127,11 +127,12 @@ __device__ __forceinline__ void st_words(void* p, const uint32_t* w) {
 // One kernel per (parameter format, state format, optimizer, gradient type).
 // A thread takes 16 consecutive elements (half a group of 32): 128-bit loads
 // and stores for a whole chunk, scalar ones for a tensor's ragged end.
-// Resident blocks per SM each instantiation is compiled for: three (at most
-// 85 registers) where the parameter is a plain bf16 or fp32 value, two (at
-// most 128) where the master is split, whose longer chains spill at 85.
+// Resident blocks per SM each instantiation is compiled for: four (at most
+// 64 registers, spilling a few hundred bytes to L1) where the parameter is a
+// plain bf16 or fp32 value, two (at most 128) where the master is split,
+// whose longer chains lose more to spills than they gain from occupancy.
 template <int PF>
-constexpr int kGenMinBlocks = (PF == FO_PARAM_BF16 || PF == FO_PARAM_F32) ? 3 : 2;
+constexpr int kGenMinBlocks = (PF == FO_PARAM_BF16 || PF == FO_PARAM_F32) ? 4 : 2;
 
 template <int PF, int SF, bool SGD, bool GB>
 __global__ void __launch_bounds__(kThreads, kGenMinBlocks<PF>) general_step_kernel(const __grid_constant__ GenArgs a) {
