@@ -61,15 +61,12 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
     return total
 
 
-# DRAM bytes (read + write) per parameter of the step kernel, from one ncu
-# capture on layer 0 of the list (profiles/adamw_step_llama3_8b_layer0_ncu.md):
-# 1.554265 GB read + 1.062396 GB written for 218,112,000 parameters.  Traffic
-# grows with the parameters processed, so a full launch is that figure times
-# the list's size.  It stands only for the kernel sources it was taken on.
 # DRAM bytes per parameter of the pipelined kernels, from one ncu capture
 # each (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the
 # 218,112,000 parameters of decoder layer 0, bf16 grads, int8 rho), keyed by
 # (kernel, format) and valid only for the kernel sources they were taken on.
+# Traffic grows with the parameters processed, so a full launch is the figure
+# times the list's size.
 _CAPTURE_SOURCES = {
     "quantized_state_optimizer_gb300/csrc/fo_step.cu": "54adec4c2e88071d273693cc91ffa708fb20c673dec6a62525daaad05a81019f",
     "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",

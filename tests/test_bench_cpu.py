@@ -1,0 +1,52 @@
+"""bench.py's accounting on the CPU: algorithmic bytes per step, the kernel a
+format runs in, and the stored DRAM-traffic captures, which must belong to the
+kernel sources in the tree (a changed kernel needs a new capture)."""
+
+import hashlib
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def test_algorithmic_bytes_of_the_8b_list():
+    numels = [s.numel for s in W.llama_tensor_list(W.LLAMA3_8B)]
+    assert sum(numels) == 8_030_261_248
+    assert bench.algorithmic_bytes(numels) == 98_370_700_288  # 12.25 B per parameter
+    # fp32 grad 4 + theta' 2 + 2 + rho 2 + 2 + codes 2 + 2 per element, and the
+    # group's two scales read and written
+    assert bench.algorithmic_bytes([32], grad_bytes=4, rho_bytes=2) == 32 * 16 + 8
+
+
+@pytest.mark.parametrize("fmt,optimizer,per_param", [
+    ("bf16_rho8:companded", "adamw", 12.25), ("bf16_rho16:linear", "adamw", 14.25),
+    ("bf16:f32", "adamw", 22.0), ("f32:f32", "adamw", 26.0),
+    ("bf16_rho8:companded", "sgd", 10.125), ("f32:f32", "sgd", 18.0),
+])
+def test_general_bytes_per_param(fmt, optimizer, per_param):
+    assert bench.general_bytes_per_param(*fmt.split(":"), optimizer) == pytest.approx(per_param)
+
+
+def test_step_kernel_routing():
+    assert bench.step_kernel_name(None, "adamw") == "fo::adamw_step_kernel"
+    assert bench.step_kernel_name("bf16_rho8:linear", "adamw") == "fo::adamw_step_kernel"
+    assert bench.step_kernel_name("bf16_rho8:companded", "adamw") == "fo::general_step_kernel"
+    assert bench.step_kernel_name("bf16_rho16:companded", "sgd") == "fo::sgd_step_kernel"
+    assert bench.step_kernel_name("bf16:linear", "sgd") == "fo::general_step_kernel"
+
+
+def test_traffic_captures_belong_to_the_kernel_sources_in_the_tree():
+    for rel, digest in bench._CAPTURE_SOURCES.items():
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            assert hashlib.sha256(fh.read()).hexdigest() == digest, (
+                f"{rel} changed since its DRAM traffic was captured: capture it again")
+    n = 8_030_261_248
+    adamw = bench.captured_traffic(n)
+    assert adamw is not None and 0.95 * 12.25 * n < adamw < 1.0 * 12.25 * n  # L2 keeps a little
+    assert bench.captured_traffic(n, "fo::sgd_step_kernel", "bf16_rho8:companded") is not None
+    assert bench.captured_traffic(n, "fo::general_step_kernel", "f32:f32") is None
