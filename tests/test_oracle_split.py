@@ -10,6 +10,8 @@ inputs for the 32-bit master, an independent binary64 rounding of the 24-bit
 master, and torch's bf16 rounding away from exact ties.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,49 +20,33 @@ import oracle as O
 import workloads as W
 
 
-def round_to_master24_f64(x: np.ndarray) -> np.ndarray:
-    """Nearest 24-bit float (15 fraction bits), ties away from zero, in binary64
-    arithmetic: multiples of 2^(E-15) for |x| in [2^E, 2^(E+1)), E >= -126;
-    the fp32 subnormal range keeps the spacing 2^-141."""
-    a = np.abs(np.asarray(x, dtype=np.float32).astype(np.float64))
-    with np.errstate(divide="ignore"):
-        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    # guard floor(log2()) at binade edges
-    e = np.where(2.0 ** e > a, e - 1, e)
-    e = np.where(2.0 ** (e + 1) <= a, e + 1, e)
-    e = np.maximum(e, -126)
-    ulp = 2.0 ** (e - 15)
-    q = np.floor(a / ulp + 0.5) * ulp
-    q = np.where(q >= 2.0 ** 128, np.inf, q)
-    return np.copysign(q, np.asarray(x, dtype=np.float64))
+from _split_ranges import round_to_master24_f64  # noqa: E402
+import _split_ranges as R  # noqa: E402
+
+
+def _over_all_patterns(fn, parts: int = 16):
+    """fn over 2^32 bit patterns cut into `parts` ranges, on a spawned pool
+    (every range is independent); the failures found."""
+    import multiprocessing as mp
+    edges = [((1 << 32) * k) // parts for k in range(parts + 1)]
+    # ranges start on multiples of 97 so the stride sample is the same as one pass
+    edges = [e - e % 97 if 0 < e < (1 << 32) else e for e in edges] if fn is R._master24_stride_range else edges
+    workers = max(1, min(parts, os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(workers) as pool:
+        out = pool.starmap(fn, [(edges[k], edges[k + 1]) for k in range(parts)])
+    return [r for r in out if r is not None]
 
 
 @pytest.mark.slow
 def test_master32_round_trip_exhaustive():
     """Every one of the 2^32 fp32 bit patterns reconstructs bit for bit
     (NaNs reconstruct as NaN)."""
-    chunk = 1 << 24
-    base = np.arange(chunk, dtype=np.uint32)
-    bits = np.empty(chunk, dtype=np.uint32)
-    for start in range(0, 1 << 32, chunk):
-        np.add(base, np.uint32(start), out=bits)
-        x = bits.view(np.float32)
-        hi, rho = O.split(x, 32)
-        back = O.reconstruct(hi, rho, 32).view(np.uint32)
-        bad = np.flatnonzero(back != bits)  # only NaN patterns may come back changed
-        assert np.all(np.isnan(x[bad])), (hex(start), bad[:5])
-        assert np.all(np.isnan(back[bad].view(np.float32))), hex(start)
+    assert _over_all_patterns(R._round_trip32_range) == []
 
 
 @pytest.mark.slow
 def test_master24_matches_binary64_rounding_exhaustive_stride():
-    bits = np.arange(0, 1 << 32, 97, dtype=np.uint64).astype(np.uint32)
-    x = bits.view(np.float32)
-    x = x[~np.isnan(x)]
-    hi, rho = O.split(x, 24)
-    back = O.reconstruct(hi, rho, 24).astype(np.float64)
-    ref = round_to_master24_f64(x)
-    assert np.array_equal(back, ref)
+    assert _over_all_patterns(R._master24_stride_range) == []
 
 
 def test_master24_on_sweep_and_bound():
