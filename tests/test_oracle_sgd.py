@@ -98,3 +98,22 @@ def test_bad_arguments():
     st.param_kind = 9
     with pytest.raises(RuntimeError):
         O.sgd_step(st, np.zeros(4, np.float32), 0.1, 0.9, 0.0, quantize_states=False)
+
+
+@pytest.mark.parametrize("master_bits", [24, 32])
+def test_momentum_zero_with_linear_codes(master_bits):
+    """Linear momentum codes: with mu = 0 theta follows plain SGD exactly as
+    with fp32 states, and the stored buffer is that step's buffer (g + wd theta,
+    which the fp32-state run holds exactly) quantized with the MOMENTUM_LINEAR
+    spec."""
+    rng = np.random.default_rng(13)
+    theta0 = (rng.standard_normal(4096 + 5) * 0.02).astype(np.float32)
+    a = O.TensorState.init(theta0, master_bits=master_bits)
+    b = O.TensorState.init(theta0, master_bits=master_bits, quantize_states=False)
+    for _ in range(3):
+        g = (rng.standard_normal(theta0.size) * 1e-3).astype(np.float32)
+        O.sgd_step(a, g, 1e-2, 0.0, 0.01, companded=False)
+        O.sgd_step(b, g, 1e-2, 0.0, 0.01, quantize_states=False)
+        assert np.array_equal(a.param, b.param) and np.array_equal(a.rho, b.rho)
+        codes, scales = O.quantize(b.m.astype(np.float32), "momentum_linear")
+        assert np.array_equal(a.m, codes) and np.array_equal(a.m_scales, scales)
