@@ -77,6 +77,29 @@ def test_first_step_closed_form(master_bits):
 
 
 @pytest.mark.parametrize("master_bits", [24, 32])
+def test_first_step_with_linear_codes(master_bits):
+    """Linear codes (companded=False): the first step's theta equals the
+    fp32-state step's bit for bit (both start from zero states), and the
+    stored codes are that step's exact m and v quantized with the
+    MOMENTUM_LINEAR / VARIANCE_LINEAR specs (v itself, no square root)."""
+    n = W.SINGLE_TENSOR_NUMEL
+    theta0 = W.single_tensor_theta(n).numpy()
+    g = W.single_tensor_grad(1, n).numpy()
+    st = O.TensorState.init(theta0, master_bits=master_bits)
+    ref = O.TensorState.init(theta0, master_bits=master_bits, quantize_states=False)
+    O.adamw_step(st, g, 1, H.lr, H.beta1, H.beta2, H.eps, H.weight_decay, companded=False)
+    O.adamw_step(ref, g, 1, H.lr, H.beta1, H.beta2, H.eps, H.weight_decay, quantize_states=False)
+    assert np.array_equal(st.param, ref.param) and np.array_equal(st.rho, ref.rho)
+    # the fp32 states are the definition's first moments, each op rounded once
+    assert np.array_equal(ref.m, np.float32(1 - H.beta1) * g)
+    assert np.array_equal(ref.v, (np.float32(1 - H.beta2) * g) * g)
+    mc, ms = O.quantize(ref.m, "momentum_linear")
+    vc, vs = O.quantize(ref.v, "variance_linear")
+    assert np.array_equal(st.m, mc) and np.array_equal(st.m_scales, ms)
+    assert np.array_equal(st.v, vc) and np.array_equal(st.v_scales, vs)
+
+
+@pytest.mark.parametrize("master_bits", [24, 32])
 def test_constant_gradient_groups_closed_form(master_bits):
     rng = np.random.default_rng(5)
     G, T = 64, 8
