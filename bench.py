@@ -33,10 +33,23 @@ import workloads as W  # noqa: E402
 
 METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) for fused AdamW step"
 UNIT = "params/s"
+# The workload: the Llama-3-8B list (24-bit master, int8 rho; the headline) or
+# the 1.1B list (32-bit master, int16 rho), chosen with --workload.
+WORKLOADS = {
+    W.LLAMA3_8B.name: (W.LLAMA3_8B, W.LLAMA3_8B_HYPER, W.LLAMA3_8B_MASTER_BITS),
+    W.TINYLLAMA_1B.name: (W.TINYLLAMA_1B, W.TINYLLAMA_HYPER, W.TINYLLAMA_MASTER_BITS),
+}
 MODEL = W.LLAMA3_8B
 HYPER = W.LLAMA3_8B_HYPER
 MASTER_BITS = W.LLAMA3_8B_MASTER_BITS
 RHO_BITS = 8 if MASTER_BITS == 24 else 16
+
+
+def use_workload(name: str) -> None:
+    """Select the tensor list, hyper-parameters and master width of a workload."""
+    global MODEL, HYPER, MASTER_BITS, RHO_BITS
+    MODEL, HYPER, MASTER_BITS = WORKLOADS[name]
+    RHO_BITS = 8 if MASTER_BITS == 24 else 16
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -44,16 +57,19 @@ def workload_config(numels) -> dict:
     return {
         "workload": (f"{MODEL.name} tensor list: {len(numels)} tensors, {sum(numels):,} params; "
                      f"bf16 theta' + int{RHO_BITS} rho ({MASTER_BITS}-bit master), int8/uint8 m/v codes "
-                     "+ fp16 group-32 scales, bf16 grads; lr 3e-4, betas (0.9, 0.95), eps 1e-8, wd 0.1"),
+                     f"+ fp16 group-32 scales, bf16 grads; lr {HYPER.lr:g}, betas ({HYPER.beta1:g}, "
+                     f"{HYPER.beta2:g}), eps {HYPER.eps:g}, wd {HYPER.weight_decay:g}"),
         "params": int(sum(numels)),
         "tensors": len(numels),
         "l2": "inputs larger than L2 (no flush needed)",
     }
 
 
-def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
+def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=None) -> int:
     """Bytes the step must move: read grad, theta', rho, m/v codes and scales;
     write theta', rho, m/v codes and scales (12.25 B/param for bf16 grad + int8 rho)."""
+    if rho_bytes is None:
+        rho_bytes = RHO_BITS // 8
     total = 0
     for n in numels:
         g = (n + 31) // 32
@@ -61,28 +77,30 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=RHO_BITS // 8) -> int:
     return total
 
 
-# DRAM bytes per parameter of the pipelined kernels, from one ncu capture
-# each (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the
-# 218,112,000 parameters of decoder layer 0, bf16 grads, int8 rho), keyed by
-# (kernel, format) and valid only for the kernel sources they were taken on.
-# Traffic grows with the parameters processed, so a full launch is the figure
-# times the list's size.
+# DRAM traffic of the pipelined kernels, from one ncu capture each
+# (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the
+# parameters of decoder layer 0, bf16 grads, int8 rho), keyed by (kernel,
+# format) and valid only for the kernel sources they were taken on.  A capture
+# on one layer reads up to one L2's worth less than the algorithmic bytes (the
+# previous launch's last tiles are still in L2); that saving is bounded by the
+# L2 size, not proportional to the launch, so it is subtracted once, not
+# scaled: a full launch moves (capture + saving) * n / n_capture - saving.
+L2_BYTES = 126 * 2**20
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "54adec4c2e88071d273693cc91ffa708fb20c673dec6a62525daaad05a81019f",
-    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "06b5fb0ab1514dd59b0731b5d0fc4ed6ad2008b392da1c32de8f03d42386e89a",
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": None,
+    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": None,
 }
-TRAFFIC_CAPTURE = {
-    ("fo::adamw_step_kernel", None): (1.554244096e9 + 1.061031680e9) / 218112000,
-    ("fo::sgd_step_kernel", "bf16_rho8:companded"): (1.322391296e9 + 0.828948992e9) / 218112000,
-}
+# (kernel, format) -> (read bytes, write bytes, parameters, algorithmic bytes per parameter)
+TRAFFIC_CAPTURE: dict = {}
 
 
 def captured_traffic(n_params: int, kernel: str = "fo::adamw_step_kernel", fmt: str | None = None) -> float | None:
-    """Per-launch DRAM traffic scaled from the capture, or None when there is
-    no capture for this kernel and format or the kernel changed since."""
+    """Per-launch DRAM traffic of a full launch over n_params, from the
+    capture, or None when there is no capture for this kernel and format or
+    the kernel changed since."""
     import hashlib
-    per_param = TRAFFIC_CAPTURE.get((kernel, fmt))
-    if per_param is None:
+    cap = TRAFFIC_CAPTURE.get((kernel, fmt))
+    if cap is None:
         return None
     for rel, digest in _CAPTURE_SOURCES.items():
         try:
@@ -91,7 +109,10 @@ def captured_traffic(n_params: int, kernel: str = "fo::adamw_step_kernel", fmt: 
                     return None
         except OSError:
             return None
-    return per_param * n_params
+    read, write, n_cap, per_param = cap
+    measured = read + write
+    saving = min(max(0.0, per_param * n_cap - measured), float(L2_BYTES))
+    return (measured + saving) * n_params / n_cap - saving
 
 
 def load_peak() -> tuple[float, str]:
@@ -530,6 +551,8 @@ def dist_env():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--workload", default=W.LLAMA3_8B.name, choices=sorted(WORKLOADS),
+                    help="tensor list: llama-3-8b (int8 rho, the headline) or llama-1.1b (int16 rho)")
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -555,6 +578,7 @@ def main():
                          "ablation format (parameter: bf16_rho8, bf16_rho16, bf16, f32; states: companded, "
                          "linear, f32) instead of the fast step")
     args = ap.parse_args()
+    use_workload(args.workload)
     ws, rank, local = dist_env()
     numels = [s.numel for s in W.llama_tensor_list(MODEL)]
 

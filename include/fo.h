@@ -255,8 +255,11 @@ fo_status fo_check_wait_timeout(uint32_t polls, void* stream);
  *   - n_tensors > FO_STATIC_MAX_TENSORS returns FO_ERR_TOO_LARGE before any
  *     other check or CUDA call.
  *   - Set-up: the first call on each device looks up the device address of
- *     the array (cudaGetSymbolAddress; FO_ERR_CUDA if that fails).  Make the
- *     first call on a device before any stream capture.
+ *     the array (cudaGetSymbolAddress) and loads every kernel variant this
+ *     entry point can launch, with its launch attributes, so that no later
+ *     call on that device loads a kernel (with lazy module loading, a
+ *     kernel's first use may allocate).  FO_ERR_CUDA if that fails.  Make
+ *     the first call on a device before any stream capture.
  *   - Each call copies the list into the array (cudaMemcpyAsync on `stream`,
  *     from pageable host memory, so the host waits until the copy has been
  *     staged) and launches on the same stream.  Nothing in the array has to

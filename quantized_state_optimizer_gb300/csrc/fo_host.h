@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "fo.h"
+#include "fo_device.cuh"
 
 namespace fo {
 
@@ -33,6 +34,16 @@ struct StepScalars {
   float c_wd, b1, one_minus_b1, b2, one_minus_b2, bc1, bc2, lr, eps;
   // constants of the approximate update: RN(lr * RN(1/bc1)) and RN(sqrt(RN(1/bc2)))
   float lr_ib1, sqrt_ib2;
+  // the exact update of the fused kernel: division by bc1 and bc2, and the
+  // gradient gate -RN(ob2 * G) (a gradient with 0 < |g| < G sends its thread
+  // to the exact IEEE chain)
+  ConstDivisor d1, d2;
+  float neg_gate;
+  float sqrt_bc2;  // RN(sqrt(bc2)): companded variance codes from the exact sqrt(v_hat)
+  float neg_zero;  // -0.0f: the addend of an exact product (RN(a b) = fma(a, b, -0))
+  // 1 when lr, eps, the betas and the bias corrections lie in the ranges the
+  // exact update is proved for; 0 sends every element to the IEEE chain
+  int fast;
 };
 StepScalars step_scalars(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
 

@@ -40,13 +40,16 @@ def test_step_kernel_routing():
     assert bench.step_kernel_name("bf16:linear", "sgd") == "fo::general_step_kernel"
 
 
-def test_traffic_captures_belong_to_the_kernel_sources_in_the_tree():
-    for rel, digest in bench._CAPTURE_SOURCES.items():
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            assert hashlib.sha256(fh.read()).hexdigest() == digest, (
-                f"{rel} changed since its DRAM traffic was captured: capture it again")
+def test_traffic_capture_is_reported_only_for_the_kernel_sources_it_was_taken_on():
     n = 8_030_261_248
+    current = all(
+        hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest() == digest
+        for rel, digest in bench._CAPTURE_SOURCES.items())
     adamw = bench.captured_traffic(n)
-    assert adamw is not None and 0.95 * 12.25 * n < adamw < 1.0 * 12.25 * n  # L2 keeps a little
-    assert bench.captured_traffic(n, "fo::sgd_step_kernel", "bf16_rho8:companded") is not None
+    if not current:
+        # the kernel changed since the capture: no traffic figure at all
+        assert adamw is None
+        return
+    # a full launch moves at least the algorithmic bytes less one L2's worth
+    assert adamw is not None and 12.25 * n - bench.L2_BYTES <= adamw < 1.01 * 12.25 * n
     assert bench.captured_traffic(n, "fo::general_step_kernel", "f32:f32") is None

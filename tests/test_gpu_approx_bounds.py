@@ -1,5 +1,6 @@
-"""The step kernel certifies results computed with rcp.approx / sqrt.approx
-against error bounds that assume at most 2 units in the last place for each.
+"""The step kernel certifies results computed with rcp.approx / sqrt.approx /
+rsqrt.approx against error bounds that assume at most 2 units in the last
+place for each.
 This measures the worst case of both over every positive normal fp32 input on
 the device in use and checks it against that assumption."""
 
@@ -22,8 +23,11 @@ def test_hardware_approximation_error_within_assumed_bound(tmp_path):
     subprocess.run([B.nvcc(), *B.ARCH, "-O3", "-Xcompiler", "-fPIC", "-shared", "-o", so,
                     os.path.join(HERE, "native", "approx_probe.cu")], check=True)
     lib = ctypes.CDLL(so)
-    out = (ctypes.c_uint * 2)()
+    out = (ctypes.c_uint * 3)()
     assert lib.approx_probe(out) == 0
-    rcp_ulp, sqrt_ulp = out[0], out[1]
-    print(f"rcp.approx.ftz max {rcp_ulp} ulp, sqrt.approx.ftz max {sqrt_ulp} ulp")
+    rcp_ulp, sqrt_ulp, rsqrt_u = out[0], out[1], out[2]
+    print(f"rcp.approx.ftz max {rcp_ulp} ulp, sqrt.approx.ftz max {sqrt_ulp} ulp, "
+          f"rsqrt.approx.ftz max relative error {rsqrt_u} * 2^-24")
     assert rcp_ulp <= ASSUMED_MAX_ULP and sqrt_ulp <= ASSUMED_MAX_ULP
+    # 2 ulp of a result in [2^k, 2^(k+1)) is at most 4 * 2^-24 relative
+    assert rsqrt_u <= 2 * ASSUMED_MAX_ULP

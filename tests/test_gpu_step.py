@@ -359,6 +359,39 @@ def test_gradient_release_matches_step():
     opt_b.remove_hooks()
 
 
+def test_gradient_release_matches_oracle():
+    """FlashAdamW(gradient_release=True) steps each parameter from its
+    post-accumulate-grad hook and frees the gradient there.  A hook registered
+    before the optimizer's captures each gradient as backward completes it;
+    the oracle steps the same gradients, and parameters, rho, codes and
+    scales must agree bit for bit after every step."""
+    net = torch.nn.Sequential(torch.nn.Linear(64, 96), torch.nn.GELU(), torch.nn.Linear(96, 48))
+    torch.manual_seed(3)
+    net = net.to(device=DEV, dtype=torch.bfloat16)
+    params = list(net.parameters())
+    refs = [O.TensorState.init(p.detach().float().cpu().numpy().reshape(-1), master_bits=24) for p in params]
+    captured = {}
+    for i, p in enumerate(params):
+        p.register_post_accumulate_grad_hook(lambda q, i=i: captured.__setitem__(i, q.grad.detach().clone()))
+    opt = FlashAdamW(params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.1, gradient_release=True)
+    for t in range(1, 4):
+        captured.clear()
+        x = torch.randn(32, 64, generator=torch.Generator().manual_seed(t)).to(DEV, torch.bfloat16)
+        (net(x).float() ** 2).mean().backward()
+        assert all(p.grad is None for p in params) and len(captured) == len(params)
+        for i, p in enumerate(params):
+            g = captured[i].reshape(-1).cpu().view(torch.int16).numpy().view(np.uint16)
+            O.adamw_step(refs[i], g, t, 1e-3, 0.9, 0.999, 1e-8, 0.1)
+        torch.cuda.synchronize()
+        for p, r in zip(params, refs):
+            s = opt.state[p]
+            got = {"param": _bits16(p.detach().reshape(-1)), "rho": s["rho"].cpu().numpy(),
+                   "m": s["m_codes"].cpu().numpy(), "m_scales": _bits16(s["m_scales"]),
+                   "v": s["v_codes"].cpu().numpy(), "v_scales": _bits16(s["v_scales"])}
+            assert_same(got, ref_np(r), ("gradient release", t))
+    opt.remove_hooks()
+
+
 def test_bounded_wait_running_out_is_reported():
     """Failure detection without a fault: a wait that nothing completes gives
     up after its poll limit, the timeout bit reaches the host through

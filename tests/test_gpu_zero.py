@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle as O
 import workloads as W
 from quantized_state_optimizer_gb300.optim import FlashAdamW, FlashAdamWState
 from quantized_state_optimizer_gb300.zero import ShardedFlashAdamWState, ZeroFlashAdamW
@@ -86,6 +87,61 @@ def test_shards_equal_the_unsharded_step(ws, rho_bits):
                 _eq(v["v_codes"], rv["v_codes"][p.start: p.end], ctx)
                 _eq(v["m_scales"], rv["m_scales"][g0: g0 + g], ctx)
                 _eq(v["v_scales"], rv["v_scales"][g0: g0 + g], ctx)
+
+
+def _bits(t):
+    return t.cpu().view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("ws", [2, 3])
+@pytest.mark.parametrize("rho_bits", [8, 16])
+def test_shards_match_the_oracle_on_summed_gradients(ws, rho_bits):
+    """Each emulated rank holds its own gradients; their sum (what the
+    reduce-scatter delivers: fp32 sum over ranks, rounded to bf16) reaches each
+    rank as its shard, and the rank steps its pieces with the fused kernel.
+    The oracle steps whole tensors with the same summed gradient; every rank's
+    pieces of rho, codes and scales, and the gathered theta', must equal the
+    oracle's elements bit for bit."""
+    h = W.LLAMA3_8B_HYPER
+    master = 24 if rho_bits == 8 else 32
+    shards = [ShardedFlashAdamWState(NUMELS, rho_bits=rho_bits, device=DEV, rank=r, world_size=ws)
+              for r in range(ws)]
+    refs = []
+    for i, n in enumerate(NUMELS):
+        th = _theta(i, n)
+        refs.append(O.TensorState.init(th.numpy(), master_bits=master))
+        for sh in shards:
+            sh.init_theta(i, th.to(DEV))
+    _gather(shards)
+    C = shards[0].layout.shard
+    for t in (1, 2, 3):
+        flat = torch.zeros(shards[0].layout.total, dtype=torch.bfloat16, device=DEV)
+        for i, n in enumerate(NUMELS):
+            local = [_grad(i + 1000 * r, t, n).float() for r in range(ws)]
+            g = torch.stack(local).sum(0).to(torch.bfloat16)
+            off = shards[0].layout.offsets[i]
+            flat[off: off + n].copy_(g.to(DEV))
+            O.adamw_step(refs[i], g.view(torch.int16).numpy().view(np.uint16), t, h.lr, h.beta1, h.beta2, h.eps,
+                         h.weight_decay)
+        for r, sh in enumerate(shards):
+            sh.grad_shard.copy_(flat[r * C: (r + 1) * C])
+            sh.step_shard(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        _gather(shards)
+        torch.cuda.synchronize()
+        for i, n in enumerate(NUMELS):
+            for sh in shards:
+                got = sh.param_view(i).cpu().view(torch.int16).numpy().view(np.uint16)
+                assert np.array_equal(got, refs[i].param), (ws, rho_bits, t, i, "param")
+        for sh in shards:
+            for p in sh.pieces:
+                v, r = sh.piece_views(p), refs[p.tensor]
+                g0, g = p.start // 32, (p.length + 31) // 32
+                ctx = (ws, rho_bits, t, sh.rank, p)
+                assert np.array_equal(_bits(v["rho"]), r.rho[p.start: p.end].view(np.uint8)), ctx
+                assert np.array_equal(_bits(v["m_codes"]), r.m[p.start: p.end].view(np.uint8)), ctx
+                assert np.array_equal(_bits(v["v_codes"]), r.v[p.start: p.end].view(np.uint8)), ctx
+                assert np.array_equal(_bits(v["m_scales"]), r.m_scales[g0: g0 + g].view(np.uint8)), ctx
+                assert np.array_equal(_bits(v["v_scales"]), r.v_scales[g0: g0 + g].view(np.uint8)), ctx
 
 
 def test_zero_optimizer_single_rank_matches_flash_adamw():

@@ -49,6 +49,32 @@ def test_unquantized_fp32_reduces_to_torch_adamw():
         assert np.max(np.abs(st.v - vr)) <= 1e-5 * np.max(np.abs(vr))
 
 
+def test_decoupled_decay_multiplies_the_old_theta_first():
+    """The page's step decays theta before the update (as torch's AdamW does).
+    With lr wd large (lr 0.1, wd 0.5) the other order, decay after the update,
+    lands lr wd |delta| away: on the first step |delta| = lr |g|/(|g| + eps)
+    ~ lr, i.e. 5e-3 for every element, far above the binary32 error of
+    either.  The oracle must match torch's order on every step, and lie that
+    far from the other order on the first."""
+    n = 1000
+    g0 = torch.Generator().manual_seed(21)
+    theta0 = (torch.randn(n, generator=g0) * 0.02).numpy().astype(np.float32)
+    lr, b1, b2, eps, wd = 0.1, 0.9, 0.999, 1e-8, 0.5
+    st = O.TensorState.init(theta0, quantize_states=False, param_dtype="f32")
+    p = torch.nn.Parameter(torch.from_numpy(theta0.astype(np.float64)))
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd, foreach=False)
+    for t in range(1, 6):
+        g = (torch.randn(n, generator=g0) * 1e-3).numpy().astype(np.float32)
+        O.adamw_step(st, g, t, lr, b1, b2, eps, wd, quantize_states=False)
+        p.grad = torch.from_numpy(g.astype(np.float64))
+        opt.step()
+        assert np.max(np.abs(st.param - p.detach().numpy())) <= 1e-5
+        if t == 1:
+            g64 = g.astype(np.float64)
+            after = (theta0 - lr * g64 / (np.abs(g64) + eps)) * (1 - lr * wd)
+            assert np.min(np.abs(st.param - after)) >= 4e-3
+
+
 @pytest.mark.parametrize("master_bits", [24, 32])
 def test_first_step_closed_form(master_bits):
     n = W.SINGLE_TENSOR_NUMEL

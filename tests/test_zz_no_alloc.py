@@ -1,7 +1,12 @@
-"""fo_adamw_step_static, the allocation-free step: through the C ABI, two
-consecutive steps must leave exactly the state that fo_adamw_step leaves on
-the same inputs.  The list is longer than one launch of fo_adamw_step
-(400 tensors), which the static entry point covers in one launch.
+"""fo_adamw_step_static, the allocation-free step, for callers that must not
+allocate device memory when they step (a loop that reserves all device
+memory for its own pools, or code running under an allocator's lock).
+Through the C ABI, two consecutive steps must leave exactly the state that
+fo_adamw_step leaves on the same inputs.  The list is longer than one launch
+of fo_adamw_step (400 tensors), which the static entry point covers in one
+launch.  After the first call on the device (its set-up), further calls, in
+another kernel variant too, must not change the device memory in use: neither
+torch's allocator statistics nor the driver's free memory.
 
 Named to be collected last; it also passes alone in a fresh process.
 """
@@ -54,6 +59,30 @@ def test_static_step_equals_fo_adamw_step(rho_bits, grad_dtype):
         for k in SLABS:
             x, y = getattr(a, k), getattr(b, k)
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), (k, t)
+    assert fo.fo_device_status() == 0
+
+
+def _memory():
+    torch.cuda.synchronize()
+    st = torch.cuda.memory_stats()
+    return (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0],
+            st.get("allocation.all.allocated", 0), st.get("segment.all.allocated", 0))
+
+
+def test_static_step_allocates_nothing_after_set_up():
+    h = W.LLAMA3_8B_HYPER
+    numels = [4096 + 17, 7680 * 3, 100]
+    a = _state(numels, 8, torch.bfloat16)
+    b = _state(numels, 16, torch.float32)  # another kernel variant (grad type, rho width, no decay)
+    _fill_grads(a, numels, 1, torch.bfloat16)
+    _fill_grads(b, numels, 1, torch.float32)
+    arr_a, arr_b = a.fo_tensors(), b.fo_tensors()
+    fo.fo_adamw_step_static(arr_a, torch.bfloat16, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, 1, 8)
+    before = _memory()
+    fo.fo_adamw_step_static(arr_a, torch.bfloat16, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, 2, 8)
+    fo.fo_adamw_step_static(arr_b, torch.float32, h.lr, h.beta1, h.beta2, h.eps, 0.0, 1, 16)
+    fo.fo_adamw_step_static(arr_b, torch.float32, h.lr, h.beta1, h.beta2, h.eps, 0.0, 2, 16)
+    assert _memory() == before
     assert fo.fo_device_status() == 0
 
 
