@@ -35,10 +35,10 @@ struct StepScalars {
   // constants of the approximate update: RN(lr * RN(1/bc1)) and RN(sqrt(RN(1/bc2)))
   float lr_ib1, sqrt_ib2;
   // the exact update of the fused kernel: division by bc1 and bc2, and the
-  // gradient gate -RN(ob2 * G) (a gradient with 0 < |g| < G sends its thread
-  // to the exact IEEE chain)
+  // gradient gate G (a gradient with 0 < |g| < G sends its thread to the
+  // exact IEEE chain)
   ConstDivisor d1, d2;
-  float neg_gate;
+  float gate;
   float sqrt_bc2;  // RN(sqrt(bc2)): companded variance codes from the exact sqrt(v_hat)
   float neg_zero;  // -0.0f: the addend of an exact product (RN(a b) = fma(a, b, -0))
   // 1 when lr, eps, the betas and the bias corrections lie in the ranges the

@@ -1,10 +1,11 @@
 // exact_probe.cu -- test helper: the correctly rounded division and square
-// root of the step kernel (fo_device.cuh: div_const, sqrt_cert, div_cert)
-// against the device's IEEE operations (__fdiv_rn, __fsqrt_rn), bit for bit,
-// over every input of their stated domains (sqrt, constant divisors) or a
-// dense structured sweep (general division).  A result whose certificate
-// failed is not compared (the step recomputes it); the number of failed
-// certificates is reported.
+// root of the step kernel (fo_device.cuh: div_const2, sqrt_cert2, div_cert2,
+// in the packed f32x2 form the kernel runs) against the device's IEEE
+// operations (__fdiv_rn, __fsqrt_rn), bit for bit, over every input of their
+// stated domains (sqrt, constant divisors) or a dense structured sweep
+// (general division).  Each thread evaluates two inputs, one per lane.  A
+// result whose certificate failed is not compared (the step recomputes it);
+// the number of failed certificates is reported.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -31,65 +32,95 @@ __device__ __forceinline__ void tally(Counts* c, unsigned long long checked, uns
   }
 }
 
-// every positive pattern (and +0) in {+0} U [2^-95, 2^100]
+// every positive pattern (and +0) in {+0} U [2^-95, 2^100]; lane y takes the
+// input half the domain above lane x's
 __global__ void sqrt_kernel(Counts* out) {
-  const uint32_t lo = 0x10000000u;  // 2^-95
-  const uint32_t hi = 0x71800000u;  // 2^100
+  const uint64_t lo = 0x10000000u;  // 2^-95
+  const uint64_t hi = 0x71800000u;  // 2^100
+  const uint64_t span = hi - lo + 2;  // +0 and the patterns lo..hi
+  const uint64_t half = (span + 1) / 2;
   unsigned long long n = 0, bad = 0, unsure = 0;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t b = (uint64_t)lo - 1 + blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; b <= hi; b += stride) {
-    const float x = b == (uint64_t)lo - 1 ? 0.0f : __uint_as_float((uint32_t)b);
-    bool ok = true;
-    const float s = fo::sqrt_cert(x, ok);
-    ++n;
-    if (!ok) ++unsure;
-    else if (__float_as_uint(s) != __float_as_uint(__fsqrt_rn(x))) ++bad;
+  auto input = [&](uint64_t i) { return i == 0 ? 0.0f : __uint_as_float((uint32_t)(lo + i - 1)); };
+  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < half; i += stride) {
+    const bool two = i + half < span;
+    const float2 x = make_float2(input(i), two ? input(i + half) : 1.0f);
+    uint32_t bx = 0, by = 0;
+    const float2 s = fo::sqrt_cert2<true>(x, bx);
+    // the lanes' certificates, told apart by running each lane's input alone too
+    fo::sqrt_cert2<true>(make_float2(x.x, x.x), bx);
+    fo::sqrt_cert2<true>(make_float2(x.y, x.y), by);
+    const bool ok[2] = {(bx >> 31) == 0, (by >> 31) == 0};
+    const float got[2] = {s.x, s.y};
+    const float in[2] = {x.x, x.y};
+    for (int l = 0; l < (two ? 2 : 1); ++l) {
+      ++n;
+      if (!ok[l]) ++unsure;
+      else if (__float_as_uint(got[l]) != __float_as_uint(__fsqrt_rn(in[l]))) ++bad;
+    }
   }
   tally(out, n, bad, unsure);
 }
 
-// every pattern with a = +0 or 2^-80 <= |a| <= 2^100, one divisor per launch
+// every pattern with a = +0 or 2^-80 <= |a| <= 2^100, one divisor per launch;
+// lane y takes the negated dividend of lane x (+0 for a = +0: -0 is outside
+// the domain)
 __global__ void div_const_kernel(ConstDivisor c, float b, Counts* out) {
   const uint32_t lo = 0x17800000u;  // 2^-80
   const uint32_t hi = 0x71800000u;  // 2^100
   const uint64_t span = (uint64_t)(hi - lo) + 1;
   unsigned long long n = 0, bad = 0;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < 2 * span + 1; i += stride) {
-    float a;
-    if (i == 2 * span) a = 0.0f;
-    else a = __uint_as_float((uint32_t)(lo + (i % span)) | (i >= span ? 0x80000000u : 0u));
-    const float q = fo::div_const(a, c);
-    ++n;
-    if (__float_as_uint(q) != __float_as_uint(__fdiv_rn(a, b))) ++bad;
+  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < span + 1; i += stride) {
+    const float a = i == span ? 0.0f : __uint_as_float((uint32_t)(lo + i));
+    const float na = i == span ? 0.0f : -a;
+    const float2 q = fo::div_const2<true>(make_float2(a, na), c);
+    n += 2;
+    if (__float_as_uint(q.x) != __float_as_uint(__fdiv_rn(a, b))) ++bad;
+    if (__float_as_uint(q.y) != __float_as_uint(__fdiv_rn(na, b))) ++bad;
   }
   tally(out, n, bad, 0);
 }
 
 // General division n / d: for each divisor d of the list, every numerator
 // significand of one binade, with an exponent that keeps the quotient in
-// range, both signs, and n = +0.
+// range, both signs, and n = +0.  Lane y divides the same numerator by the
+// divisor half the list further on.
+__device__ __forceinline__ float div_numerator(const float* divisors, int k, uint32_t r) {
+  const float d = divisors[k];
+  // numerator exponent: spread over [-80, 69] by the divisor index, then
+  // clipped so that |n/d| >= 2^-101
+  int e = -80 + (int)((k * 37) % 150);
+  const int ed = (int)((__float_as_uint(d) >> 23) & 0xFF) - 127;
+  if (e - ed < -100) e = ed - 100;
+  const uint32_t bits = ((uint32_t)(e + 127) << 23) | (r & 0x7FFFFFu) | ((r >> 23) << 31);
+  return (r == 0 && (k & 1)) ? 0.0f : __uint_as_float(bits);
+}
 __global__ void div_cert_kernel(const float* divisors, int nd, Counts* out) {
   unsigned long long n = 0, bad = 0, unsure = 0;
   const uint64_t per = (uint64_t)1 << 24;  // 2^23 significands x 2 signs
-  const uint64_t total = per * (uint64_t)nd;
+  const int halfd = (nd + 1) / 2;
+  const uint64_t total = per * (uint64_t)halfd;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int k = (int)(i / per);
+    const int k0 = (int)(i / per);
+    const int k1 = k0 + halfd;
+    const bool two = k1 < nd;
     const uint32_t r = (uint32_t)(i % per);
-    const float d = divisors[k];
-    // numerator exponent: spread over [-80, 69] by the divisor index, then
-    // clipped so that |n/d| >= 2^-101
-    int e = -80 + (int)((k * 37) % 150);
-    const int ed = (int)((__float_as_uint(d) >> 23) & 0xFF) - 127;
-    if (e - ed < -100) e = ed - 100;
-    const uint32_t bits = ((uint32_t)(e + 127) << 23) | (r & 0x7FFFFFu) | ((r >> 23) << 31);
-    const float num = (r == 0 && (k & 1)) ? 0.0f : __uint_as_float(bits);
-    bool ok = true;
-    const float q = fo::div_cert(num, d, ok);
+    const float n0 = div_numerator(divisors, k0, r), d0 = divisors[k0];
+    const float n1 = two ? div_numerator(divisors, k1, r) : 1.0f, d1 = two ? divisors[k1] : 1.0f;
+    uint32_t b = 0, bx = 0, by = 0;
+    const float2 q = fo::div_cert2<true>(make_float2(n0, n1), make_float2(d0, d1), b);
+    fo::div_cert2<true>(make_float2(n0, n0), make_float2(d0, d0), bx);
+    fo::div_cert2<true>(make_float2(n1, n1), make_float2(d1, d1), by);
     ++n;
-    if (!ok) ++unsure;
-    else if (__float_as_uint(q) != __float_as_uint(__fdiv_rn(num, d))) ++bad;
+    if (bx >> 31) ++unsure;
+    else if (__float_as_uint(q.x) != __float_as_uint(__fdiv_rn(n0, d0))) ++bad;
+    if (two) {
+      ++n;
+      if (by >> 31) ++unsure;
+      else if (__float_as_uint(q.y) != __float_as_uint(__fdiv_rn(n1, d1))) ++bad;
+    }
   }
   tally(out, n, bad, unsure);
 }

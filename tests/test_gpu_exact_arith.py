@@ -1,7 +1,7 @@
 """The fused step's correctly rounded division and square root (fo_device.cuh:
-div_const, sqrt_cert, div_cert: a hardware approximation, FMA residuals and
-one rounding, after Markstein) against the device's IEEE division and square
-root, bit for bit:
+div_const2, sqrt_cert2, div_cert2 in their packed f32x2 form: a hardware
+approximation, FMA residuals and one rounding, after Markstein) against the
+device's IEEE division and square root, bit for bit:
 
 - the square root over every input of its domain (+0 and [2^-95, 2^100]);
 - division by a launch constant over every dividend of its domain, for the

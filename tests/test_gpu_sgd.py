@@ -149,12 +149,12 @@ def test_sgd_volume_heavy_tailed(pf, sf):
     _run_sgd([(1 << 22) + 5, 3 * (1 << 20)], pf, torch.bfloat16, 1e-2, 0.9, 0.05, 4, grad_fn, theta_fn, sf=sf)
 
 
-def test_sgd_half_integer_codes_overflow_the_redo_queue():
+def test_sgd_half_integer_codes_leave_every_certificate_open():
     """On the first step the buffer is the gradient itself.  Gradients chosen
     so that every element but the group maximum 1.0 has a code argument
     127 * 2y/(1+y) next to a half-integer k + 1/2 (y = (k + 1/2)/(254 - k - 1/2),
-    rounded to fp32) leave nearly every code uncertain: far more per tile than
-    the redo queue holds, so the in-thread exact path runs as well."""
+    rounded to fp32) leave nearly every code certificate open, so nearly every
+    thread finishes through the exact path."""
     k = np.arange(31) * 4 + 0.5
     y = (k / (254.0 - k)).astype(np.float32)
     group = np.concatenate([[np.float32(1.0)], y]).astype(np.float32)
