@@ -223,15 +223,20 @@ def general_bytes_per_param(pf: str, sf: str, optimizer: str = "adamw") -> float
 
 class PerTensorSteps:
     """The step as gradient release issues it: one single-tensor
-    ``fo_adamw_step`` launch per tensor (what ``FlashAdamW(gradient_release=
-    True)`` launches from each parameter's post-accumulate-grad hook), here
-    back to back on one stream."""
+    ``fo_adamw_step`` launch per tensor of at least ``bucket`` elements (what
+    ``FlashAdamW(gradient_release=True)`` launches from each parameter's
+    post-accumulate-grad hook) and one launch for all smaller tensors (its
+    bucket of small parameters), here back to back on one stream."""
 
-    def __init__(self, st):
+    def __init__(self, st, bucket: int = 1 << 20):
         from quantized_state_optimizer_gb300 import FoTensor
         full = st.fo_tensors()
         self.st = st
-        self.arrs = [(FoTensor * 1)(full[i]) for i in range(len(st.numels))]
+        big = [i for i, n in enumerate(st.numels) if n >= bucket]
+        small = [i for i, n in enumerate(st.numels) if n < bucket]
+        self.arrs = [(FoTensor * 1)(full[i]) for i in big]
+        if small:
+            self.arrs.append((FoTensor * len(small))(*[full[i] for i in small]))
 
     def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
         from quantized_state_optimizer_gb300 import fo_adamw_step
@@ -624,6 +629,7 @@ def main():
     st, numels = build_state(device, args.layers, args.format, args.optimizer)
     stream = torch.cuda.Stream(device=device)
     stepper = PerTensorSteps(st) if args.per_tensor else st
+    launches_per_step = len(stepper.arrs) if args.per_tensor else 1
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(stepper, args.steps, args.warmup, stream, dist_on)
     ms = max_over_ranks(total_ms / args.steps, device)
@@ -689,7 +695,7 @@ def main():
                                  if args.layers is None and not args.per_tensor else None)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (len(numels) if args.per_tensor else 1),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

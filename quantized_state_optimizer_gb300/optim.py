@@ -205,34 +205,84 @@ class FlashAdamW(torch.optim.Optimizer):
     the parameter's gradient is complete and then frees the gradient, so no
     gradient outlives its own update (the ``gradient_release`` accounting of
     ``bytes_per_param`` on the page "code/flashsim/flash_adamw_sim.py").
-    ``step()`` is then a no-op for those parameters.  The result equals a
-    normal step on the same gradients bit for bit: every tensor's update is
-    independent of the others.
+    Parameters of fewer than ``release_bucket_numel`` elements (norm weights,
+    say) are gathered instead: their group's bucket is stepped in one launch
+    once every such parameter of the group has its gradient, or at
+    ``step()`` for any left over, so those few small gradients live until
+    their bucket's update.  ``step()`` does nothing else for released
+    parameters.  The result equals a normal step on the same gradients bit
+    for bit: every tensor's update is independent of the others.
     """
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0,
-                 master_weight_bits: int = 24, gradient_release: bool = False):
+                 master_weight_bits: int = 24, gradient_release: bool = False,
+                 release_bucket_numel: int = 1 << 20):
         if master_weight_bits not in (24, 32):
             raise ValueError("master_weight_bits must be 24 or 32")
         defaults = dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay)
         super().__init__(params, defaults)
         self.rho_bits = 8 if master_weight_bits == 24 else 16
         self.gradient_release = gradient_release
+        self.release_bucket_numel = int(release_bucket_numel)
         self._hooks = []
+        self._args = {}     # parameter -> its one-entry fo_tensor array (state pointers fixed)
+        self._pending = {}  # group index -> small parameters whose gradients are complete
+        self._n_small = {}  # group index -> number of small parameters in the group
         if gradient_release:
-            for group in self.param_groups:
+            for gi, group in enumerate(self.param_groups):
+                small = [p for p in group["params"] if p.numel() < self.release_bucket_numel]
+                self._n_small[gi] = len(small)
                 for p in group["params"]:
-                    self._hooks.append(p.register_post_accumulate_grad_hook(self._release_hook(group)))
+                    self._hooks.append(p.register_post_accumulate_grad_hook(self._release_hook(gi, group)))
 
-    def _release_hook(self, group):
+    def _release_hook(self, gi: int, group):
         def hook(p: torch.Tensor) -> None:
+            if p.numel() < self.release_bucket_numel:
+                pend = self._pending.setdefault(gi, [])
+                pend.append(p)
+                if len(pend) == self._n_small[gi]:
+                    self._flush(gi)
+                return
             with torch.no_grad():
-                self._step_params(group, [p])
+                self._step_one(group, p)
             p.grad = None
         return hook
 
+    def _flush(self, gi: int) -> None:
+        """Step a group's gathered small parameters in one launch and free their gradients."""
+        pend = self._pending.pop(gi, [])
+        if pend:
+            with torch.no_grad():
+                self._step_params(self.param_groups[gi], pend)
+            for p in pend:
+                p.grad = None
+
+    def _step_one(self, group, p: torch.Tensor) -> None:
+        """The single-tensor step of a released parameter through its cached argument array."""
+        st = self.state[p]
+        if len(st) == 0:
+            st = self._init_state(p)
+        arr = self._args.get(p)
+        if arr is None:
+            arr = (FoTensor * 1)(FoTensor(p.data_ptr(), st["rho"].data_ptr(), 0, st["m_codes"].data_ptr(),
+                                          st["m_scales"].data_ptr(), st["v_codes"].data_ptr(),
+                                          st["v_scales"].data_ptr(), p.numel()))
+            self._args[p] = arr
+        st["step"] += 1
+        g = p.grad if p.grad.is_contiguous() else p.grad.contiguous()
+        arr[0].grad = g.data_ptr()
+        beta1, beta2 = group["betas"]
+        fo_adamw_step(arr, g.dtype, group["lr"], beta1, beta2, group["eps"], group["weight_decay"], st["step"],
+                      self.rho_bits)
+
+    def load_state_dict(self, state_dict) -> None:
+        super().load_state_dict(state_dict)
+        self._args = {}  # the state buffers were replaced
+
     def remove_hooks(self) -> None:
         """Detach the gradient-release hooks (the optimizer then steps in ``step()``)."""
+        for gi in list(self._pending):
+            self._flush(gi)
         for h in self._hooks:
             h.remove()
         self._hooks = []
@@ -262,6 +312,9 @@ class FlashAdamW(torch.optim.Optimizer):
         if not self.gradient_release:
             for group in self.param_groups:
                 self._step_params(group, group["params"])
+        else:
+            for gi in list(self._pending):  # small parameters whose bucket did not fill
+                self._flush(gi)
         return loss
 
     def _step_params(self, group, params) -> None:

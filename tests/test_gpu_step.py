@@ -253,12 +253,25 @@ def test_torch_optimizer_front_end_matches_oracle():
         assert_same(got, ref_np(r), "FlashAdamW")
 
 
-def test_zero_initialized_weights_overflow_the_redo_queue():
-    """theta = 0 makes the new theta equal to -delta, whose 24-bit master is
-    uncertain for about one element in eight -- more per tile than the redo
-    queue holds, so the in-thread exact path runs too."""
+def test_zero_initialized_weights():
+    """theta = 0: the new theta is -delta itself, so the master carries every
+    bit of the update (no bits of an old theta to round into)."""
     numels = [7680 * 4, 7680 * 2 + 33]
     run_small(numels, 8, torch.bfloat16, W.LLAMA3_8B_HYPER, 3, theta_fn=lambda i, n: torch.zeros(n))
+
+
+@pytest.mark.parametrize("rho_bits", [8, 16])
+def test_cancelling_update(rho_bits):
+    """theta = lr sign(g): the first step's update nearly cancels theta, so the
+    new theta is a small difference of two close values (tiny, subnormal-free
+    results whose low bits all come from delta)."""
+    h = W.LLAMA3_8B_HYPER
+    numels = [7680 * 3 + 17]
+
+    def theta_fn(i, n):
+        return torch.sign(_grad(i, 1, n, torch.bfloat16).float()) * h.lr
+
+    run_small(numels, rho_bits, torch.bfloat16, h, 2, theta_fn)
 
 
 def test_device_status_clear_after_steps():
@@ -327,10 +340,13 @@ def test_llama3_8b_list_int8_rho_20_steps_sampled():
     assert st.total_numel() == 8_030_261_248 and len(st) == 291
 
 
-def test_gradient_release_matches_step():
+@pytest.mark.parametrize("bucket", [0, 5000, 1 << 20])
+def test_gradient_release_matches_step(bucket):
     """FlashAdamW(gradient_release=True) steps each parameter inside backward
     and frees its gradient; parameters and states equal those of the normal
-    step on the same gradients, bit for bit."""
+    step on the same gradients, bit for bit.  bucket = 0 steps every
+    parameter alone, 5000 gathers the biases and the 96 x 48 weight into one
+    launch, 2^20 gathers all four."""
     torch.manual_seed(0)
 
     def model():
@@ -340,7 +356,8 @@ def test_gradient_release_matches_step():
 
     a, b = model(), model()
     opt_a = FlashAdamW(a.parameters(), lr=1e-3, weight_decay=0.1)
-    opt_b = FlashAdamW(b.parameters(), lr=1e-3, weight_decay=0.1, gradient_release=True)
+    opt_b = FlashAdamW(b.parameters(), lr=1e-3, weight_decay=0.1, gradient_release=True,
+                       release_bucket_numel=bucket)
     for t in range(3):
         x = torch.randn(32, 64, generator=torch.Generator().manual_seed(t)).to(DEV, torch.bfloat16)
         (a(x).float() ** 2).mean().backward()
@@ -359,7 +376,41 @@ def test_gradient_release_matches_step():
     opt_b.remove_hooks()
 
 
-def test_gradient_release_matches_oracle():
+def test_gradient_release_bucket_left_open_is_stepped_by_step():
+    """A small parameter that gets no gradient keeps its bucket from filling:
+    the other small parameters keep their gradients through backward and
+    step() steps them, equal to the normal step bit for bit."""
+    def model():
+        torch.manual_seed(1)
+        return torch.nn.Sequential(torch.nn.Linear(64, 96), torch.nn.GELU(), torch.nn.Linear(96, 48)).to(
+            device=DEV, dtype=torch.bfloat16)
+
+    a, b = model(), model()
+    unused = torch.nn.Parameter(torch.zeros(16, dtype=torch.bfloat16, device=DEV))
+    opt_a = FlashAdamW(a.parameters(), lr=1e-3, weight_decay=0.1)
+    opt_b = FlashAdamW(list(b.parameters()) + [unused], lr=1e-3, weight_decay=0.1, gradient_release=True,
+                       release_bucket_numel=5000)
+    for t in range(2):
+        x = torch.randn(32, 64, generator=torch.Generator().manual_seed(10 + t)).to(DEV, torch.bfloat16)
+        (a(x).float() ** 2).mean().backward()
+        opt_a.step()
+        opt_a.zero_grad(set_to_none=True)
+        (b(x).float() ** 2).mean().backward()
+        held = [p.grad is not None for p in b.parameters()]
+        assert held == [False, True, True, True]  # the 64 x 96 weight alone was released
+        opt_b.step()
+        assert all(p.grad is None for p in b.parameters()) and unused.grad is None
+        torch.cuda.synchronize()
+        for pa, pb in zip(a.parameters(), b.parameters()):
+            assert torch.equal(pa.view(torch.int16), pb.view(torch.int16)), t
+            for k in ("rho", "m_codes", "m_scales", "v_codes", "v_scales"):
+                assert torch.equal(opt_a.state[pa][k].view(torch.uint8), opt_b.state[pb][k].view(torch.uint8))
+    assert len(opt_b.state[unused]) == 0
+    opt_b.remove_hooks()
+
+
+@pytest.mark.parametrize("bucket", [0, 1 << 20])
+def test_gradient_release_matches_oracle(bucket):
     """FlashAdamW(gradient_release=True) steps each parameter from its
     post-accumulate-grad hook and frees the gradient there.  A hook registered
     before the optimizer's captures each gradient as backward completes it;
@@ -373,7 +424,8 @@ def test_gradient_release_matches_oracle():
     captured = {}
     for i, p in enumerate(params):
         p.register_post_accumulate_grad_hook(lambda q, i=i: captured.__setitem__(i, q.grad.detach().clone()))
-    opt = FlashAdamW(params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.1, gradient_release=True)
+    opt = FlashAdamW(params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.1, gradient_release=True,
+                     release_bucket_numel=bucket)
     for t in range(1, 4):
         captured.clear()
         x = torch.randn(32, 64, generator=torch.Generator().manual_seed(t)).to(DEV, torch.bfloat16)
