@@ -169,6 +169,40 @@ def test_volume_heavy_tailed_parity(rho_bits):
             assert_same(gpu_view_np(st, i), ref_np(refs[i]), ("volume", rho_bits, i, t))
 
 
+@pytest.mark.parametrize("rho_bits", [8, 16])
+def test_groups_with_subnormal_scales_beside_normal_ones(rho_bits):
+    """Each group of 32 gets its own gradient magnitude, from 1e-9 to 1e-2:
+    tiny groups have subnormal or zero fp16 scales (their code arguments can
+    pass the code range and need the clamps), the others normal ones (the
+    clamp-free form), side by side in every warp."""
+    numels = [7680 * 2 + 4096 + 96, 33 * 32 + 5]
+    h = W.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, steps=3)
+    mb = 24 if rho_bits == 8 else 32
+    st = FlashAdamWState(numels, rho_bits=rho_bits, grad_dtype=torch.bfloat16, device=DEV)
+    refs = []
+    for i, n in enumerate(numels):
+        theta = torch.randn(n, generator=torch.Generator().manual_seed(40 + i)) * 0.02
+        st.init_theta(i, theta.to(DEV))
+        refs.append(O.TensorState.init(theta.numpy(), master_bits=mb))
+    for t in range(1, h.steps + 1):
+        for i, n in enumerate(numels):
+            gen = torch.Generator().manual_seed(W.grad_seed(91, i, t))
+            groups = (n + 31) // 32
+            mag = 10.0 ** -torch.randint(2, 10, (groups,), generator=gen).double()
+            g = (torch.randn(n, generator=gen).double() * mag.repeat_interleave(32)[:n]).float().to(torch.bfloat16)
+            st.grad_view(i).copy_(g.to(DEV))
+            O.adamw_step(refs[i], g.view(torch.int16).numpy().view(np.uint16), t, h.lr, h.beta1, h.beta2,
+                         h.eps, h.weight_decay)
+        st.step(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay)
+        torch.cuda.synchronize()
+        for i in range(len(numels)):
+            got = gpu_view_np(st, i)
+            assert_same(got, ref_np(refs[i]), ("subnormal scales", rho_bits, i, t))
+    # both kinds of scale occurred
+    ms = np.abs(st.m_scales.float().cpu().numpy())
+    assert np.any((ms > 0) & (ms < 2.0 ** -14)) and np.any(ms >= 2.0 ** -14)
+
+
 def test_checkpoint_resume_is_bit_identical():
     numels = [5000, 4096, 77]
     h = W.TINYLLAMA_HYPER
