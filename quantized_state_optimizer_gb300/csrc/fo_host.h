@@ -53,11 +53,11 @@ StepScalars step_scalars(double lr, double beta1, double beta2, double eps, doub
 fo_status launch_sgd_fast(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits, bool companded,
                           double lr, double momentum, double weight_decay, cudaStream_t s);
 
-// AdamW with linear codes and a split master through the pipelined step
-// kernel; the list must already have passed the checks of
+// AdamW with companded or linear codes and a split master through the
+// pipelined step kernel; the list must already have passed the checks of
 // fo_adamw_step_general.
-fo_status launch_adamw_linear(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits,
-                              double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step,
-                              cudaStream_t s);
+fo_status launch_adamw_split(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits,
+                             bool companded, double lr, double beta1, double beta2, double eps, double weight_decay,
+                             int64_t step, cudaStream_t s);
 
 }  // namespace fo

@@ -384,10 +384,12 @@ GenKernel gen_kernel_sf(int sf, bool gb) {
          : sf == FO_STATE_LINEAR  ? gen_kernel<PF, FO_STATE_LINEAR, SGD>(gb)
                                   : gen_kernel<PF, FO_STATE_F32, SGD>(gb);
 }
+// A split master with codes runs in the pipelined kernel (fo_step.cu); here
+// only its fp32-state form.
 template <bool SGD>
 GenKernel gen_kernel_pf(int pf, int sf, bool gb) {
-  return pf == FO_PARAM_BF16_RHO8    ? gen_kernel_sf<FO_PARAM_BF16_RHO8, SGD>(sf, gb)
-         : pf == FO_PARAM_BF16_RHO16 ? gen_kernel_sf<FO_PARAM_BF16_RHO16, SGD>(sf, gb)
+  return pf == FO_PARAM_BF16_RHO8    ? gen_kernel<FO_PARAM_BF16_RHO8, FO_STATE_F32, SGD>(gb)
+         : pf == FO_PARAM_BF16_RHO16 ? gen_kernel<FO_PARAM_BF16_RHO16, FO_STATE_F32, SGD>(gb)
          : pf == FO_PARAM_BF16       ? gen_kernel_sf<FO_PARAM_BF16, SGD>(sf, gb)
                                      : gen_kernel_sf<FO_PARAM_F32, SGD>(sf, gb);
 }
@@ -511,11 +513,11 @@ extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int
   if (step < 1) return FO_ERR_INVALID_ARG;
   if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
   if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return FO_ERR_INVALID_ARG;
-  // linear codes with a split master: the pipelined kernel (the companded
-  // ones stay here, where they cross-check fo_adamw_step)
-  if (state_format == FO_STATE_LINEAR && (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
-    return launch_adamw_linear(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
-                               lr, beta1, beta2, eps, weight_decay, step, as_stream(stream));
+  // codes with a split master: the pipelined kernel
+  if (state_format != FO_STATE_F32 && (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
+    return launch_adamw_split(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
+                              state_format == FO_STATE_COMPANDED, lr, beta1, beta2, eps, weight_decay, step,
+                              as_stream(stream));
   GenArgs args;
   args.k = step_scalars(lr, beta1, beta2, eps, weight_decay, step);
   args.sgd = 0;

@@ -35,7 +35,8 @@ def test_general_bytes_per_param(fmt, optimizer, per_param):
 def test_step_kernel_routing():
     assert bench.step_kernel_name(None, "adamw") == "fo::adamw_step_kernel"
     assert bench.step_kernel_name("bf16_rho8:linear", "adamw") == "fo::adamw_step_kernel"
-    assert bench.step_kernel_name("bf16_rho8:companded", "adamw") == "fo::general_step_kernel"
+    assert bench.step_kernel_name("bf16_rho8:companded", "adamw") == "fo::adamw_step_kernel"
+    assert bench.step_kernel_name("bf16_rho8:f32", "adamw") == "fo::general_step_kernel"
     assert bench.step_kernel_name("bf16_rho16:companded", "sgd") == "fo::sgd_step_kernel"
     assert bench.step_kernel_name("bf16:linear", "sgd") == "fo::general_step_kernel"
 

@@ -129,7 +129,10 @@ def test_general_step_matches_oracle(pf, sf, grad_dtype):
 
 
 @pytest.mark.parametrize("rho_bits", [8, 16])
-def test_general_kernel_equals_fast_kernel_in_the_papers_format(rho_bits):
+def test_general_entry_equals_fo_adamw_step_in_the_papers_format(rho_bits):
+    """fo_adamw_step_general in the paper's format (split master, companded
+    codes) runs the pipelined kernel of fo_adamw_step through its own argument
+    path: the same bits."""
     from quantized_state_optimizer_gb300.optim import FlashAdamWState
     numels = [70000, 4096 * 5 + 3, 31]
     h = W.LLAMA3_8B_HYPER
