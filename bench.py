@@ -77,29 +77,35 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=None) -> int:
     return total
 
 
-# DRAM traffic of the pipelined kernels, from one ncu capture each
+# DRAM traffic of the pipelined kernel, from one ncu capture each
 # (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the
-# parameters of decoder layer 0, bf16 grads, int8 rho), keyed by (kernel,
-# format) and valid only for the kernel sources they were taken on.  A capture
+# parameters of decoder layer 0, bf16 grads), keyed by (kernel, format, rho
+# width) and valid only for the kernel sources they were taken on.  A capture
 # on one layer reads up to one L2's worth less than the algorithmic bytes (the
 # previous launch's last tiles are still in L2); that saving is bounded by the
 # L2 size, not proportional to the launch, so it is subtracted once, not
 # scaled: a full launch moves (capture + saving) * n / n_capture - saving.
 L2_BYTES = 126 * 2**20
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": None,
-    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": None,
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "3f68ad9ffa8637618ff3fe0f0419a505428f4679ab632f168be7cd8c0adf863c",
+    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "72f96197501e7bf722400e3391daaf1b3d2aac458e637eb051b827c0236aba87",
 }
-# (kernel, format) -> (read bytes, write bytes, parameters, algorithmic bytes per parameter)
-TRAFFIC_CAPTURE: dict = {}
+# (kernel, format, rho bits) -> (read bytes, write bytes, parameters, algorithmic bytes per parameter)
+TRAFFIC_CAPTURE: dict = {
+    # 8B list, layer 0 (9 tensors), int8 rho
+    ("fo::adamw_step_kernel", None, 8): (1_554_226_000, 1_059_769_000, 218_112_000, 12.25),
+    # 1.1B list, layer 0 (9 tensors), int16 rho
+    ("fo::adamw_step_kernel", None, 16): (357_984_256, 212_419_072, 44_044_288, 14.25),
+}
 
 
-def captured_traffic(n_params: int, kernel: str = "fo::adamw_step_kernel", fmt: str | None = None) -> float | None:
+def captured_traffic(n_params: int, kernel: str = "fo::adamw_step_kernel", fmt: str | None = None,
+                     rho_bits: int | None = None) -> float | None:
     """Per-launch DRAM traffic of a full launch over n_params, from the
     capture, or None when there is no capture for this kernel and format or
     the kernel changed since."""
     import hashlib
-    cap = TRAFFIC_CAPTURE.get((kernel, fmt))
+    cap = TRAFFIC_CAPTURE.get((kernel, fmt, RHO_BITS if rho_bits is None else rho_bits))
     if cap is None:
         return None
     for rel, digest in _CAPTURE_SOURCES.items():
