@@ -251,14 +251,14 @@ class PerTensorSteps:
 
 
 def step_kernel_name(fmt: str | None, optimizer: str) -> str:
-    """The kernel one step launches: the pipelined kernel for a split master
+    """The kernel one step launches: the pipelined kernel for every format
     with companded or linear codes (AdamW through fo_adamw_step or
-    fo_adamw_step_general, SGD through fo_sgd_step), else the general kernel."""
+    fo_adamw_step_general, SGD through fo_sgd_step), else (fp32 states) the
+    general kernel."""
     if fmt is None:
         return "fo::adamw_step_kernel"
-    pf, sf = fmt.split(":")
-    split = pf in ("bf16_rho8", "bf16_rho16")
-    if split and sf in ("companded", "linear"):
+    sf = fmt.split(":")[1]
+    if sf in ("companded", "linear"):
         return "fo::sgd_step_kernel" if optimizer == "sgd" else "fo::adamw_step_kernel"
     return "fo::general_step_kernel"
 

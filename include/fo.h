@@ -167,10 +167,11 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
  * Every result is the exact binary32 definition: divisions and square roots
  * correctly rounded from certified approximations, codes, the 24-bit master
  * and a bf16 parameter without a split certified, each with the IEEE chain
- * as fallback (the same bits).  The two FO_PARAM_BF16_RHO* formats with codes
- * (companded or linear) run in fo_adamw_step's pipelined kernel, which
- * reports a bounded wait that ran out through fo_device_status(); with
- * FO_STATE_COMPANDED the call gives fo_adamw_step's bits.
+ * as fallback (the same bits).  Every format with codes (companded or
+ * linear) runs in fo_adamw_step's pipelined kernel, which reports a bounded
+ * wait that ran out through fo_device_status(); a split master with
+ * FO_STATE_COMPANDED gives fo_adamw_step's bits.  The fp32-state formats run
+ * in a separate, simpler kernel.
  * Buffers as in fo_tensor, with widths by format: param 2 or 4 bytes per
  * element, rho 1 or 2 (unused, may be NULL, without a split), m and v 1 byte
  * (codes) or 4 (fp32), m_scales / v_scales fp16 [ceil(numel/32)] (unused, may

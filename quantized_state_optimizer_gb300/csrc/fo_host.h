@@ -47,16 +47,17 @@ struct StepScalars {
 };
 StepScalars step_scalars(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
 
-// SGD with momentum with a split master (bf16 theta' with int8 or int16 rho)
-// and companded or linear momentum codes, through the pipelined step kernel;
-// the list must already have passed the checks of fo_sgd_step.
+// SGD with momentum (companded or linear momentum codes) through the
+// pipelined step kernel, for the parameter format rho_bits (8 or 16: a split
+// master; 0: a bf16 parameter; 32: an fp32 parameter); the list must already
+// have passed the checks of fo_sgd_step.
 fo_status launch_sgd_fast(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits, bool companded,
                           double lr, double momentum, double weight_decay, cudaStream_t s);
 
-// AdamW with companded or linear codes and a split master through the
-// pipelined step kernel; the list must already have passed the checks of
-// fo_adamw_step_general.
-fo_status launch_adamw_split(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits,
+// AdamW with companded or linear codes through the pipelined step kernel, for
+// the parameter format rho_bits (as above); the list must already have passed
+// the checks of fo_adamw_step_general.
+fo_status launch_adamw_fused(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits,
                              bool companded, double lr, double beta1, double beta2, double eps, double weight_decay,
                              int64_t step, cudaStream_t s);
 

@@ -384,14 +384,20 @@ GenKernel gen_kernel_sf(int sf, bool gb) {
          : sf == FO_STATE_LINEAR  ? gen_kernel<PF, FO_STATE_LINEAR, SGD>(gb)
                                   : gen_kernel<PF, FO_STATE_F32, SGD>(gb);
 }
-// A split master with codes runs in the pipelined kernel (fo_step.cu); here
-// only its fp32-state form.
+// Formats with codes run in the pipelined kernel (fo_step.cu); here only the
+// fp32-state forms.
 template <bool SGD>
 GenKernel gen_kernel_pf(int pf, int sf, bool gb) {
+  (void)sf;
   return pf == FO_PARAM_BF16_RHO8    ? gen_kernel<FO_PARAM_BF16_RHO8, FO_STATE_F32, SGD>(gb)
          : pf == FO_PARAM_BF16_RHO16 ? gen_kernel<FO_PARAM_BF16_RHO16, FO_STATE_F32, SGD>(gb)
-         : pf == FO_PARAM_BF16       ? gen_kernel_sf<FO_PARAM_BF16, SGD>(sf, gb)
-                                     : gen_kernel_sf<FO_PARAM_F32, SGD>(sf, gb);
+         : pf == FO_PARAM_BF16       ? gen_kernel<FO_PARAM_BF16, FO_STATE_F32, SGD>(gb)
+                                     : gen_kernel<FO_PARAM_F32, FO_STATE_F32, SGD>(gb);
+}
+
+// The pipelined kernel's parameter format (its kRhoBits) of a format.
+int fused_param_format(int pf) {
+  return pf == FO_PARAM_BF16_RHO8 ? 8 : pf == FO_PARAM_BF16_RHO16 ? 16 : pf == FO_PARAM_BF16 ? 0 : 32;
 }
 GenKernel select_general_kernel(const GenArgs& a) {
   return a.sgd ? gen_kernel_pf<true>(a.param_format, a.state_format, a.grad_bf16)
@@ -513,9 +519,9 @@ extern "C" fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int
   if (step < 1) return FO_ERR_INVALID_ARG;
   if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
   if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return FO_ERR_INVALID_ARG;
-  // codes with a split master: the pipelined kernel
-  if (state_format != FO_STATE_F32 && (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
-    return launch_adamw_split(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
+  // every format with codes: the pipelined kernel
+  if (state_format != FO_STATE_F32)
+    return launch_adamw_fused(tensors, n_tensors, grad_dtype == FO_DT_BF16, fused_param_format(param_format),
                               state_format == FO_STATE_COMPANDED, lr, beta1, beta2, eps, weight_decay, step,
                               as_stream(stream));
   GenArgs args;
@@ -536,8 +542,8 @@ extern "C" fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors
   fo_status st = check_general(tensors, n_tensors, param_format, state_format, grad_dtype, false);
   if (st != FO_OK) return st;
   if (!std::isfinite(lr) || !std::isfinite(momentum) || !std::isfinite(weight_decay)) return FO_ERR_INVALID_ARG;
-  if (state_format != FO_STATE_F32 && (param_format == FO_PARAM_BF16_RHO8 || param_format == FO_PARAM_BF16_RHO16))
-    return launch_sgd_fast(tensors, n_tensors, grad_dtype == FO_DT_BF16, param_format == FO_PARAM_BF16_RHO8 ? 8 : 16,
+  if (state_format != FO_STATE_F32)
+    return launch_sgd_fast(tensors, n_tensors, grad_dtype == FO_DT_BF16, fused_param_format(param_format),
                            state_format == FO_STATE_COMPANDED, lr, momentum, weight_decay, as_stream(stream));
   GenArgs args;
   args.k = step_scalars(lr, 0.0, 0.0, 1.0, 0.0, 1);  // only k.lr is used: RN(lr)

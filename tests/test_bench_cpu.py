@@ -38,7 +38,9 @@ def test_step_kernel_routing():
     assert bench.step_kernel_name("bf16_rho8:companded", "adamw") == "fo::adamw_step_kernel"
     assert bench.step_kernel_name("bf16_rho8:f32", "adamw") == "fo::general_step_kernel"
     assert bench.step_kernel_name("bf16_rho16:companded", "sgd") == "fo::sgd_step_kernel"
-    assert bench.step_kernel_name("bf16:linear", "sgd") == "fo::general_step_kernel"
+    assert bench.step_kernel_name("bf16:linear", "sgd") == "fo::sgd_step_kernel"
+    assert bench.step_kernel_name("f32:companded", "adamw") == "fo::adamw_step_kernel"
+    assert bench.step_kernel_name("f32:f32", "sgd") == "fo::general_step_kernel"
 
 
 def test_traffic_capture_is_reported_only_for_the_kernel_sources_it_was_taken_on():
