@@ -200,21 +200,93 @@ def bench_specs(layers: int | None):
 
 
 def build_state(device, layers: int | None = None, fmt: str | None = None, optimizer: str = "adamw"):
+    """The state of the list (θ from the input recipe, zero states) with the
+    gradients drawn for step 1 in its own grad slab, and the further
+    gradient sets (``grad_sets(...)``) that the timed steps cycle through."""
     from quantized_state_optimizer_gb300.optim import FlashAdamWState
-    all_specs = W.llama_tensor_list(MODEL)
     specs = bench_specs(layers)
     numels = [s.numel for s in specs]
-    wid = W.WORKLOAD_IDS[MODEL.name]
     if fmt is not None:
         st = GeneralState(numels, *fmt.split(":"), device, optimizer)
     else:
         st = FlashAdamWState(numels, rho_bits=RHO_BITS, grad_dtype=torch.bfloat16, device=device)
-    for i, s in enumerate(specs):
-        k = all_specs.index(s)  # seeds follow the tensor's index in the full list
-        st.init_theta(i, W.init_theta(s, wid, k, device))
-        W.make_grad(s.numel, wid, k, 1, device, out=st.grad_view(i))
+    wid = W.WORKLOAD_IDS[MODEL.name]
+    for i, k in enumerate(tensor_indices(specs)):
+        st.init_theta(i, W.init_theta(specs[i], wid, k, device))
+        W.make_grad(specs[i].numel, wid, k, 1, device, out=st.grad_view(i))
     torch.cuda.synchronize()
     return st, numels
+
+
+def tensor_indices(specs) -> list[int]:
+    """Each tensor's index in the full list (the seeds follow it)."""
+    all_specs = W.llama_tensor_list(MODEL)
+    return [all_specs.index(s) for s in specs]
+
+
+# Resident gradient sets the timed steps cycle through: step t reads the set
+# drawn for step 1 + (t - 1) mod GRAD_SETS.  A gradient that never changes
+# drives m and v towards values with few significant bits, which no training
+# run sees; drawing a new one inside the timed region would time the input
+# generator.
+GRAD_SETS = 2
+
+
+def grad_sets(st, layers: int | None, device) -> list[torch.Tensor]:
+    """The grad slabs of steps 1..GRAD_SETS in the layout of ``st.grad``:
+    ``st.grad`` itself (drawn by ``build_state``) and the later ones."""
+    specs = bench_specs(layers)
+    wid = W.WORKLOAD_IDS[MODEL.name]
+    slabs = [st.grad]
+    for step in range(2, GRAD_SETS + 1):
+        slab = torch.zeros_like(st.grad)
+        for i, k in enumerate(tensor_indices(specs)):
+            v = st.grad_view(i)
+            o = v.storage_offset() - st.grad.storage_offset()
+            W.make_grad(specs[i].numel, wid, k, step, device, out=slab[o:o + v.numel()])
+        slabs.append(slab)
+    torch.cuda.synchronize()
+    return slabs
+
+
+class BenchSteps:
+    """The timed step: step t launches over gradient set (t - 1) mod
+    len(slabs).  By default one launch per step over every tensor.  With
+    ``per_tensor`` it issues the step as gradient release launches it: one
+    single-tensor ``fo_adamw_step`` launch per tensor of at least ``bucket``
+    elements (what ``FlashAdamW(gradient_release=True)`` launches from each
+    parameter's post-accumulate-grad hook) and one launch for all smaller
+    tensors (its bucket of small parameters), here back to back on one
+    stream."""
+
+    def __init__(self, st, slabs, per_tensor: bool = False, bucket: int = 1 << 20):
+        self.st = st
+        self.general = isinstance(st, GeneralState)
+        self.sets = []
+        for slab in slabs:
+            full = st.grad_array(slab) if self.general else st.fo_tensors(
+                grads=[slab[st.grad_view(i).storage_offset() - st.grad.storage_offset():][:n]
+                       for i, n in enumerate(st.numels)])
+            if not per_tensor:
+                self.sets.append([full])
+                continue
+            ctype = type(full[0])
+            big = [i for i, n in enumerate(st.numels) if n >= bucket]
+            small = [i for i, n in enumerate(st.numels) if n < bucket]
+            arrs = [(ctype * 1)(full[i]) for i in big]
+            if small:
+                arrs.append((ctype * len(small))(*[full[i] for i in small]))
+            self.sets.append(arrs)
+        self.launches_per_step = len(self.sets[0])
+
+    def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
+        import quantized_state_optimizer_gb300 as fo
+        for arr in self.sets[(t - 1) % len(self.sets)]:
+            if self.general:
+                self.st.launch(arr, t, lr, beta1, beta2, eps, weight_decay, stream)
+            else:
+                fo.fo_adamw_step(arr, self.st.grad_dtype, lr, beta1, beta2, eps, weight_decay, t,
+                                 self.st.rho_bits, stream)
 
 
 # ------------------------------------------------- the ablation formats
@@ -227,40 +299,11 @@ def general_bytes_per_param(pf: str, sf: str, optimizer: str = "adamw") -> float
     return 2 + 2 * param + 2 * rho + (2 if optimizer == "adamw" else 1) * one_state
 
 
-class PerTensorSteps:
-    """The step as gradient release issues it: one single-tensor
-    ``fo_adamw_step`` launch per tensor of at least ``bucket`` elements (what
-    ``FlashAdamW(gradient_release=True)`` launches from each parameter's
-    post-accumulate-grad hook) and one launch for all smaller tensors (its
-    bucket of small parameters), here back to back on one stream."""
-
-    def __init__(self, st, bucket: int = 1 << 20):
-        from quantized_state_optimizer_gb300 import FoTensor
-        full = st.fo_tensors()
-        self.st = st
-        big = [i for i, n in enumerate(st.numels) if n >= bucket]
-        small = [i for i, n in enumerate(st.numels) if n < bucket]
-        self.arrs = [(FoTensor * 1)(full[i]) for i in big]
-        if small:
-            self.arrs.append((FoTensor * len(small))(*[full[i] for i in small]))
-
-    def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
-        from quantized_state_optimizer_gb300 import fo_adamw_step
-        for arr in self.arrs:
-            fo_adamw_step(arr, self.st.grad_dtype, lr, beta1, beta2, eps, weight_decay, t, self.st.rho_bits, stream)
-
-
 def step_kernel_name(fmt: str | None, optimizer: str) -> str:
-    """The kernel one step launches: the pipelined kernel for every format
-    with companded or linear codes (AdamW through fo_adamw_step or
-    fo_adamw_step_general, SGD through fo_sgd_step), else (fp32 states) the
-    general kernel."""
-    if fmt is None:
-        return "fo::adamw_step_kernel"
-    sf = fmt.split(":")[1]
-    if sf in ("companded", "linear"):
-        return "fo::sgd_step_kernel" if optimizer == "sgd" else "fo::adamw_step_kernel"
-    return "fo::general_step_kernel"
+    """The kernel one step launches: the pipelined step kernel in every
+    format (AdamW through fo_adamw_step or fo_adamw_step_general, SGD
+    through fo_sgd_step)."""
+    return "fo::sgd_step_kernel" if optimizer == "sgd" else "fo::adamw_step_kernel"
 
 
 class GeneralState:
@@ -290,14 +333,21 @@ class GeneralState:
         self.ms = None if sf == "f32" else torch.zeros(gtotal, dtype=torch.float16, device=device)
         self.vs = None if sf == "f32" else torch.zeros(gtotal, dtype=torch.float16, device=device)
         self.grad = torch.zeros(total, dtype=torch.bfloat16, device=device)
+        self.goffs = goffs
+        self.arr = self.grad_array(self.grad)
+
+    def grad_array(self, grad: torch.Tensor):
+        """``fo_tensor_general`` array over the slabs, reading gradients from ``grad``."""
+        import quantized_state_optimizer_gb300 as fo
         ptr = lambda t, off, esz: t.data_ptr() + off * esz if t is not None else None  # noqa: E731
-        self.arr = (fo.FoTensorGeneral * len(numels))(*[
+        offs, goffs = self.offs, self.goffs
+        return (fo.FoTensorGeneral * len(self.numels))(*[
             fo.FoTensorGeneral(ptr(self.param, offs[i], self.param.element_size()),
                                ptr(self.rho, offs[i], self.rho.element_size() if self.rho is not None else 0),
-                               ptr(self.grad, offs[i], 2), ptr(self.m, offs[i], self.m.element_size()),
+                               ptr(grad, offs[i], 2), ptr(self.m, offs[i], self.m.element_size()),
                                ptr(self.ms, goffs[i], 2), ptr(self.v, offs[i], self.v.element_size()),
                                ptr(self.vs, goffs[i], 2), n)
-            for i, n in enumerate(numels)])
+            for i, n in enumerate(self.numels)])
 
     def init_theta(self, i: int, theta: torch.Tensor) -> None:
         import quantized_state_optimizer_gb300 as fo
@@ -311,11 +361,14 @@ class GeneralState:
         return self.grad[self.offs[i]:self.offs[i] + self.numels[i]]
 
     def step(self, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
+        self.launch(self.arr, t, lr, beta1, beta2, eps, weight_decay, stream)
+
+    def launch(self, arr, t, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
         import quantized_state_optimizer_gb300 as fo
         if self.optimizer == "sgd":  # momentum beta1, the same lr and weight decay
-            fo.fo_sgd_step(self.arr, self.pf, self.sf, torch.bfloat16, lr, beta1, weight_decay, stream)
+            fo.fo_sgd_step(arr, self.pf, self.sf, torch.bfloat16, lr, beta1, weight_decay, stream)
         else:
-            fo.fo_adamw_step_general(self.arr, self.pf, self.sf, torch.bfloat16, lr, beta1, beta2, eps,
+            fo.fo_adamw_step_general(arr, self.pf, self.sf, torch.bfloat16, lr, beta1, beta2, eps,
                                      weight_decay, t, stream)
 
 
@@ -631,9 +684,10 @@ def main():
     if args.optimizer == "sgd" and args.format is None:
         args.format = "bf16_rho8:companded"
     st, numels = build_state(device, args.layers, args.format, args.optimizer)
+    slabs = grad_sets(st, args.layers, device)
     stream = torch.cuda.Stream(device=device)
-    stepper = PerTensorSteps(st) if args.per_tensor else st
-    launches_per_step = len(stepper.arrs) if args.per_tensor else 1
+    stepper = BenchSteps(st, slabs, per_tensor=args.per_tensor)
+    launches_per_step = stepper.launches_per_step
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(stepper, args.steps, args.warmup, stream, dist_on)
     ms = max_over_ranks(total_ms / args.steps, device)
@@ -656,7 +710,7 @@ def main():
     except RuntimeError as exc:  # e.g. pinned host memory unavailable: keep the device number
         e2e = {"value": None, "unit": UNIT, "error": str(exc).splitlines()[0][:200]}
     footprint = st.bytes_allocated() if hasattr(st, "bytes_allocated") else None
-    del st, stepper
+    del st, stepper, slabs
     torch.cuda.empty_cache()
 
     if rank != 0:

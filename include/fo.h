@@ -167,11 +167,10 @@ fo_status fo_adamw_step(const fo_tensor* tensors, int n_tensors, fo_dtype grad_d
  * Every result is the exact binary32 definition: divisions and square roots
  * correctly rounded from certified approximations, codes, the 24-bit master
  * and a bf16 parameter without a split certified, each with the IEEE chain
- * as fallback (the same bits).  Every format with codes (companded or
- * linear) runs in fo_adamw_step's pipelined kernel, which reports a bounded
- * wait that ran out through fo_device_status(); a split master with
- * FO_STATE_COMPANDED gives fo_adamw_step's bits.  The fp32-state formats run
- * in a separate, simpler kernel.
+ * as fallback (the same bits).  Every format runs in fo_adamw_step's
+ * pipelined kernel, which reports a bounded wait that ran out through
+ * fo_device_status(); a split master with FO_STATE_COMPANDED gives
+ * fo_adamw_step's bits.
  * Buffers as in fo_tensor, with widths by format: param 2 or 4 bytes per
  * element, rho 1 or 2 (unused, may be NULL, without a split), m and v 1 byte
  * (codes) or 4 (fp32), m_scales / v_scales fp16 [ceil(numel/32)] (unused, may
@@ -211,12 +210,10 @@ fo_status fo_adamw_step_general(const fo_tensor_general* tensors, int n_tensors,
  * = the MOMENTUM spec, FO_STATE_LINEAR = MOMENTUM_LINEAR, FO_STATE_F32 = fp32);
  * v and v_scales are unused (may be NULL).  All-zero codes and scales are the
  * initial buffer, so the first step stores buf = g as torch does.
- * In the paper's format (FO_PARAM_BF16_RHO8 or FO_PARAM_BF16_RHO16 with
- * FO_STATE_COMPANDED) the step runs in the pipelined kernel of fo_adamw_step,
- * one HBM pass, momentum codes certified from a hardware reciprocal with the
- * exact chain as fallback (the same bits); other formats run the kernel of
- * fo_adamw_step_general.  Same errors as fo_adamw_step_general; the pipelined kernel also
- * reports a bounded wait that ran out through fo_device_status(). */
+ * Every format runs in the pipelined kernel of fo_adamw_step, one HBM pass,
+ * momentum codes certified from a hardware reciprocal with the exact chain
+ * as fallback (the same bits).  Same errors as fo_adamw_step_general; a
+ * bounded wait that ran out is reported through fo_device_status(). */
 fo_status fo_sgd_step(const fo_tensor_general* tensors, int n_tensors, fo_param_format param_format,
                       fo_state_format state_format, fo_dtype grad_dtype, double lr, double momentum,
                       double weight_decay, void* stream);

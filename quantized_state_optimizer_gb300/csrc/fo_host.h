@@ -47,18 +47,22 @@ struct StepScalars {
 };
 StepScalars step_scalars(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
 
-// SGD with momentum (companded or linear momentum codes) through the
-// pipelined step kernel, for the parameter format rho_bits (8 or 16: a split
-// master; 0: a bf16 parameter; 32: an fp32 parameter); the list must already
-// have passed the checks of fo_sgd_step.
-fo_status launch_sgd_fast(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits, bool companded,
+// State formats of a pipelined launch: companded codes, linear codes, or
+// fp32 states without scales.
+constexpr int kStatesCompanded = 0, kStatesLinear = 1, kStatesF32 = 2;
+
+// SGD with momentum through the pipelined step kernel, for the parameter
+// format rho_bits (8 or 16: a split master; 0: a bf16 parameter; 32: an fp32
+// parameter) and the state format `states`; the list must already have
+// passed the checks of fo_sgd_step.
+fo_status launch_sgd_fast(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits, int states,
                           double lr, double momentum, double weight_decay, cudaStream_t s);
 
-// AdamW with companded or linear codes through the pipelined step kernel, for
-// the parameter format rho_bits (as above); the list must already have passed
-// the checks of fo_adamw_step_general.
+// AdamW through the pipelined step kernel, for the parameter and state
+// formats as above; the list must already have passed the checks of
+// fo_adamw_step_general.
 fo_status launch_adamw_fused(const fo_tensor_general* tensors, int n_tensors, bool grad_bf16, int rho_bits,
-                             bool companded, double lr, double beta1, double beta2, double eps, double weight_decay,
+                             int states, double lr, double beta1, double beta2, double eps, double weight_decay,
                              int64_t step, cudaStream_t s);
 
 }  // namespace fo

@@ -36,11 +36,11 @@ def test_step_kernel_routing():
     assert bench.step_kernel_name(None, "adamw") == "fo::adamw_step_kernel"
     assert bench.step_kernel_name("bf16_rho8:linear", "adamw") == "fo::adamw_step_kernel"
     assert bench.step_kernel_name("bf16_rho8:companded", "adamw") == "fo::adamw_step_kernel"
-    assert bench.step_kernel_name("bf16_rho8:f32", "adamw") == "fo::general_step_kernel"
+    assert bench.step_kernel_name("bf16_rho8:f32", "adamw") == "fo::adamw_step_kernel"
     assert bench.step_kernel_name("bf16_rho16:companded", "sgd") == "fo::sgd_step_kernel"
     assert bench.step_kernel_name("bf16:linear", "sgd") == "fo::sgd_step_kernel"
     assert bench.step_kernel_name("f32:companded", "adamw") == "fo::adamw_step_kernel"
-    assert bench.step_kernel_name("f32:f32", "sgd") == "fo::general_step_kernel"
+    assert bench.step_kernel_name("f32:f32", "sgd") == "fo::sgd_step_kernel"
 
 
 def test_traffic_capture_is_reported_only_for_the_kernel_sources_it_was_taken_on():
@@ -55,4 +55,4 @@ def test_traffic_capture_is_reported_only_for_the_kernel_sources_it_was_taken_on
         return
     # a full launch moves at least the algorithmic bytes less one L2's worth
     assert adamw is not None and 12.25 * n - bench.L2_BYTES <= adamw < 1.01 * 12.25 * n
-    assert bench.captured_traffic(n, "fo::general_step_kernel", "f32:f32") is None
+    assert bench.captured_traffic(n, "fo::adamw_step_kernel", "f32:f32") is None
