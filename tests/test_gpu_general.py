@@ -197,3 +197,60 @@ def test_linear_codes_split_master_pipelined(pf, grad_dtype):
             for key, ref in (("param", r.param), ("rho", r.rho), ("m", r.m), ("v", r.v), ("ms", r.m_scales),
                              ("vs", r.v_scales)):
                 _same(got[key], ref, ctx + (key,))
+
+
+def _tie_grads(n: int, sf: str, seed: int) -> torch.Tensor:
+    """fp32 gradients for one step with beta1 = 1/2, beta2 = 0 (m = g/2
+    exactly, v = RN(g^2)) under which nearly every code argument lies within
+    about 1e-6 of a half-integer.  Element 0 of each group of 32 is g = 2: the
+    momentum scale becomes 1, the variance scale 2 (companded: fp16 of
+    sqrt(4)) or 4 (linear).  Even elements tie the momentum code t = k + 1/2:
+    m = t/(254 - t) (companded, the inverse softsign of t/127) or t/127
+    (linear).  Odd elements tie the variance code: |g| = 2t/255 (companded:
+    t = 255 sqrt(v)/2) or 2 sqrt(t/255) (linear: t = 255 v/4)."""
+    rng = np.random.default_rng(seed)
+    g = np.empty(n, np.float64)
+    sign = rng.choice([-1.0, 1.0], n)
+    k_m = rng.integers(0, 127, n) + 0.5
+    k_v = rng.integers(0, 255, n) + 0.5
+    m_tie = k_m / (254.0 - k_m) if sf == "companded" else k_m / 127.0
+    v_tie = 2.0 * k_v / 255.0 if sf == "companded" else 2.0 * np.sqrt(k_v / 255.0)
+    idx = np.arange(n)
+    g[:] = np.where(idx % 2 == 0, 2.0 * m_tie, v_tie)
+    g[idx % 32 == 0] = 2.0
+    return torch.from_numpy((sign * g).astype(np.float32))
+
+
+@pytest.mark.parametrize("sf", ["companded", "linear"])
+@pytest.mark.parametrize("pf", ["bf16_rho8", "bf16_rho16", "bf16", "f32"])
+def test_code_arguments_on_half_integer_ties(pf, sf):
+    """Code arguments a hair from a half-integer in nearly every element: the
+    kernel's certified codes cannot decide them, so every pair of every thread
+    takes its codes from the definition's chain out of line; the rest of the
+    step stays on the fast path.  Full tiles and a ragged tail, bit for bit
+    against the oracle."""
+    h = W.Hyper(lr=1e-3, beta1=0.5, beta2=0.0, eps=1e-8, weight_decay=0.05, steps=1)
+    numels = [3 * 11776 + 1000, 4096]
+    thetas = [_theta(10 + i, n) for i, n in enumerate(numels)]
+    dev = [DevTensor(t, pf, sf, torch.float32) for t in thetas]
+    refs = [_oracle_state(t, pf, sf) for t in thetas]
+    arr = (FoTensorGeneral * len(dev))(*[d.ft() for d in dev])
+    for i, n in enumerate(numels):
+        g = _tie_grads(n, sf, 77 + i)
+        dev[i].grad.copy_(g.to(DEV))
+        O.adamw_step(refs[i], g.numpy(), 1, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay,
+                     quantize_states=True, companded=sf == "companded")
+    fo.fo_adamw_step_general(arr, pf, sf, torch.float32, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, 1)
+    torch.cuda.synchronize()
+    for i, n in enumerate(numels):
+        got, r = dev[i].host(), refs[i]
+        ctx = (pf, sf, i)
+        _same(got["param"], r.param, ctx + ("param",))
+        if r.rho is not None:
+            _same(got["rho"], r.rho, ctx + ("rho",))
+        for k, rk in (("m", r.m), ("v", r.v), ("ms", r.m_scales), ("vs", r.v_scales)):
+            _same(got[k], rk, ctx + (k,))
+        # the construction did what it says: scales 1 and 2 (or 4), and the
+        # tied codes split between the two neighbours of each half-integer
+        assert np.all(r.m_scales == np.float16(1.0).view(np.uint16))
+        assert np.all(r.v_scales == np.float16(2.0 if sf == "companded" else 4.0).view(np.uint16))
