@@ -87,15 +87,15 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=None) -> int:
 # scaled: a full launch moves (capture + saving) * n / n_capture - saving.
 L2_BYTES = 126 * 2**20
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "3f68ad9ffa8637618ff3fe0f0419a505428f4679ab632f168be7cd8c0adf863c",
-    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "72f96197501e7bf722400e3391daaf1b3d2aac458e637eb051b827c0236aba87",
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "80ca4d747dab345b81862a0dfa9b63573c1cdbffcac72e286c9708ed27b7cf59",
+    "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "96c6ebfe451225a7fd564d8bc375e13a2922dc028e2148557970f44fd83a4964",
 }
 # (kernel, format, rho bits) -> (read bytes, write bytes, parameters, algorithmic bytes per parameter)
 TRAFFIC_CAPTURE: dict = {
     # 8B list, layer 0 (9 tensors), int8 rho
-    ("fo::adamw_step_kernel", None, 8): (1_554_226_000, 1_059_769_000, 218_112_000, 12.25),
+    ("fo::adamw_step_kernel", None, 8): (1_563_076_000, 1_072_759_000, 218_112_000, 12.25),
     # 1.1B list, layer 0 (9 tensors), int16 rho
-    ("fo::adamw_step_kernel", None, 16): (357_984_256, 212_419_072, 44_044_288, 14.25),
+    ("fo::adamw_step_kernel", None, 16): (361_646_336, 215_432_448, 44_044_288, 14.25),
 }
 
 
