@@ -39,7 +39,7 @@ struct StepScalars {
   // exact IEEE chain)
   ConstDivisor d1, d2;
   float gate;
-  float sqrt_bc2;  // RN(sqrt(bc2)): companded variance codes from the exact sqrt(v_hat)
+  float c255_root_bc2;  // RN(255 sqrt(bc2)): companded variance codes from the exact sqrt(v_hat)
   float neg_zero;  // -0.0f: the addend of an exact product (RN(a b) = fma(a, b, -0))
   // 1 when lr, eps, the betas and the bias corrections lie in the ranges the
   // exact update is proved for; 0 sends every element to the IEEE chain
