@@ -401,25 +401,31 @@ def time_steps(st, steps: int, warmup: int, stream, dist_on: bool) -> tuple[floa
     return total_ms, per
 
 
-def time_e2e(st, numels, steps: int, stream) -> dict:
+def time_e2e(st, numels, steps: int, stream, slabs) -> dict:
     """Same step through the public API with host buffers: each step uploads the
     bf16 grads from pinned host memory and downloads the updated bf16
     parameters into pinned host memory (``FlashAdamWState.step_from_host``,
     which overlaps both copies with the step chunk by chunk), all inside the
-    timed region."""
+    timed region.  The host holds the gradient sets of the device bench
+    (``slabs``) and step t uploads set (t - 1) mod len(slabs)."""
     h = HYPER
-    host_grad = torch.empty(st.grad.numel(), dtype=st.grad.dtype, pin_memory=True)
-    host_grad.copy_(st.grad)
+    host_grads = []
+    for slab in slabs:
+        hg = torch.empty(slab.numel(), dtype=slab.dtype, pin_memory=True)
+        hg.copy_(slab)
+        host_grads.append(hg)
     host_param = torch.empty(st.param.numel(), dtype=st.param.dtype, pin_memory=True)
     torch.cuda.synchronize()
     t = 1000
-    st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param, stream=stream)
+    st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grads[(t - 1) % len(host_grads)],
+                      host_param, stream=stream)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ev[0].record(stream)
     for k in range(steps):
         t += 1
-        st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grad, host_param, stream=stream)
+        st.step_from_host(t, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, host_grads[(t - 1) % len(host_grads)],
+                          host_param, stream=stream)
         ev[k + 1].record(stream)
     torch.cuda.synchronize()
     per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
@@ -427,7 +433,7 @@ def time_e2e(st, numels, steps: int, stream) -> dict:
     n = sum(numels)
     return {"value": n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
             "ms_per_step_min": min(per), "ms_per_step_median": statistics.median(per), "ms_per_step_max": max(per),
-            "h2d_bytes_per_step": int(host_grad.numel() * host_grad.element_size()),
+            "h2d_bytes_per_step": int(host_grads[0].numel() * host_grads[0].element_size()),
             "d2h_bytes_per_step": int(host_param.numel() * host_param.element_size()),
             "steps": steps, "api": "FlashAdamWState.step_from_host (8 chunks, copies overlapped)"}
 
@@ -699,7 +705,7 @@ def main():
     peak, peak_kind = load_peak()
     achieved = bytes_step / (kernel_ms * 1e-3) / 1e9
     try:
-        e2e = (time_e2e(st, numels, args.e2e_steps, stream)
+        e2e = (time_e2e(st, numels, args.e2e_steps, stream, slabs)
                if args.e2e_steps > 0 and args.format is None and not args.per_tensor else None)
         if e2e is not None:
             # the link's own ceiling on this machine, for reading the e2e number

@@ -56,3 +56,42 @@ def test_traffic_capture_is_reported_only_for_the_kernel_sources_it_was_taken_on
     # a full launch moves at least the algorithmic bytes less one L2's worth
     assert adamw is not None and 12.25 * n - bench.L2_BYTES <= adamw < 1.01 * 12.25 * n
     assert bench.captured_traffic(n, "fo::adamw_step_kernel", "f32:f32") is None
+
+
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_bench_steps_cycle_the_gradient_sets(per_tensor):
+    """Step t of the timed loop launches over gradient set (t - 1) mod 2: every
+    tensor's grad pointer lies in that set's slab at the tensor's own offset,
+    and the other state pointers are the same in both sets.  Host memory only;
+    nothing is launched."""
+    import torch
+    from quantized_state_optimizer_gb300.optim import FlashAdamWState
+    numels = [100, 3000, (1 << 20) + 5, 4096, 7]
+    st = FlashAdamWState(numels, rho_bits=8, device="cpu")
+    slabs = [st.grad, torch.zeros_like(st.grad)]
+    steps = bench.BenchSteps(st, slabs, per_tensor=per_tensor)
+    full = st.fo_tensors()
+    big = [i for i, n in enumerate(numels) if n >= 1 << 20]
+    small = [i for i, n in enumerate(numels) if n < 1 << 20]
+    order = (big + small) if per_tensor else list(range(len(numels)))
+    assert steps.launches_per_step == (len(big) + 1 if per_tensor else 1)
+    for t in (1, 2, 3, 4):
+        k = (t - 1) % 2
+        launched = [ft for arr in steps.sets[k] for ft in arr]
+        assert len(launched) == len(numels)
+        for ft, i in zip(launched, order):
+            off = st.grad_view(i).storage_offset() * st.grad.element_size()
+            assert ft.grad == slabs[k].data_ptr() + off
+            assert (ft.param, ft.rho, ft.m_codes, ft.v_codes, ft.numel) == \
+                (full[i].param, full[i].rho, full[i].m_codes, full[i].v_codes, full[i].numel)
+
+
+def test_general_state_gradient_sets():
+    """The ablation-format state builds its argument array for any grad slab."""
+    import torch
+    st = bench.GeneralState([33, 4096, 5], "f32", "linear", "cpu")
+    other = torch.zeros_like(st.grad)
+    arr = st.grad_array(other)
+    for i, n in enumerate(st.numels):
+        assert arr[i].grad == other.data_ptr() + st.offs[i] * 2
+        assert arr[i].param == st.arr[i].param and arr[i].numel == n
