@@ -87,7 +87,7 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=None) -> int:
 # scaled: a full launch moves (capture + saving) * n / n_capture - saving.
 L2_BYTES = 126 * 2**20
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "44a153756a08eeac7a23acddf4f3177c72c79c05145365663de083c1e47bffb9",
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "62c0b48d312094f3bec3b1ee4a03789dc1afa666f128fffe29513a61e154a5bd",
     "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "0f67b3354cfa65905708fe4d4c4bf24a285c2c36db7f160db62129242a2f1373",
 }
 # (kernel, format, rho bits) -> (read bytes, write bytes, parameters, algorithmic bytes per parameter)
