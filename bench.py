@@ -87,15 +87,15 @@ def algorithmic_bytes(numels, grad_bytes=2, rho_bytes=None) -> int:
 # scaled: a full launch moves (capture + saving) * n / n_capture - saving.
 L2_BYTES = 126 * 2**20
 _CAPTURE_SOURCES = {
-    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "62c0b48d312094f3bec3b1ee4a03789dc1afa666f128fffe29513a61e154a5bd",
+    "quantized_state_optimizer_gb300/csrc/fo_step.cu": "7763e84c6e2c76f2a38afd4fd8a7456b1bfe1532987d74ada1c0cf0a38e5821b",
     "quantized_state_optimizer_gb300/csrc/fo_device.cuh": "0f67b3354cfa65905708fe4d4c4bf24a285c2c36db7f160db62129242a2f1373",
 }
 # (kernel, format, rho bits) -> (read bytes, write bytes, parameters, algorithmic bytes per parameter)
 TRAFFIC_CAPTURE: dict = {
     # 8B list, layer 0 (9 tensors), int8 rho
-    ("fo::adamw_step_kernel", None, 8): (1_565_652_000, 1_074_564_000, 218_112_000, 12.25),
+    ("fo::adamw_step_kernel", None, 8): (1_565_242_000, 1_074_010_000, 218_112_000, 12.25),
     # 1.1B list, layer 0 (9 tensors), int16 rho
-    ("fo::adamw_step_kernel", None, 16): (361_993_472, 216_884_224, 44_044_288, 14.25),
+    ("fo::adamw_step_kernel", None, 16): (361_392_384, 215_593_984, 44_044_288, 14.25),
 }
 
 
