@@ -39,6 +39,7 @@ WORKLOADS = {
     W.LLAMA3_8B.name: (W.LLAMA3_8B, W.LLAMA3_8B_HYPER, W.LLAMA3_8B_MASTER_BITS),
     W.TINYLLAMA_1B.name: (W.TINYLLAMA_1B, W.TINYLLAMA_HYPER, W.TINYLLAMA_MASTER_BITS),
 }
+SINGLE = "single-65553"
 MODEL = W.LLAMA3_8B
 HYPER = W.LLAMA3_8B_HYPER
 MASTER_BITS = W.LLAMA3_8B_MASTER_BITS
@@ -443,6 +444,51 @@ def time_e2e(st, numels, steps: int, stream, slabs) -> dict:
             "steps": steps, "api": "FlashAdamWState.step_from_host (8 chunks, copies overlapped)"}
 
 
+def single_tensor_line(steps: int, warmup: int, device) -> dict:
+    """The single-tensor workload: 65,553 parameters, fp32 grads (seed 1000 + t,
+    the ten steps of the input recipe cycled), int8 rho, lr 1e-3, betas (0.9,
+    0.999), eps 1e-8, wd 0.01.  Its 0.93 MB fit in L2, so one step is bound by
+    launch and pipeline latency: no roofline claim."""
+    from quantized_state_optimizer_gb300 import fo_adamw_step
+    from quantized_state_optimizer_gb300.optim import FlashAdamWState
+    n = W.SINGLE_TENSOR_NUMEL
+    h = W.SINGLE_TENSOR_HYPER
+    st = FlashAdamWState([n], rho_bits=8, grad_dtype=torch.float32, device=device)
+    st.init_theta(0, W.single_tensor_theta(n).to(device))
+    grads = [W.single_tensor_grad(t, n).to(device) for t in range(1, h.steps + 1)]
+    arrs = [st.fo_tensors(grads=[g]) for g in grads]
+    stream = torch.cuda.Stream(device=device)
+
+    def step(t):
+        fo_adamw_step(arrs[(t - 1) % len(arrs)], torch.float32, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, t, 8,
+                      stream)
+
+    t = 0
+    for _ in range(warmup):
+        t += 1
+        step(t)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for k in range(steps):
+        t += 1
+        step(t)
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    ms = ev[0].elapsed_time(ev[steps]) / steps
+    return {"metric": METRIC, "value": n / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": warmup,
+            "ms_per_step": ms, "ms_per_step_median": statistics.median(per), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": (f"single tensor: {n:,} params, fp32 grads (ten seeded steps, cycled), bf16 "
+                                    f"theta' + int8 rho (24-bit master), lr {h.lr:g}, betas ({h.beta1:g}, "
+                                    f"{h.beta2:g}), eps {h.eps:g}, wd {h.weight_decay:g}"),
+                       "params": n, "tensors": 1,
+                       "l2": "0.93 MB fit in L2: latency-bound, no roofline claim",
+                       "bytes_per_step": algorithmic_bytes([n], grad_bytes=4)},
+            "roofline": None, "cpu_baseline": None, "e2e": None, "gpu_launches": steps}
+
+
 # ------------------------------------------------------------ CPU oracle
 def oracle_sample(total_params: int, chunk: int = 1 << 20, seed: int = 1, layers: int = 2):
     """A bounded, seeded sample of the workload for the CPU oracle: group-aligned
@@ -624,8 +670,9 @@ def dist_env():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--workload", default=W.LLAMA3_8B.name, choices=sorted(WORKLOADS),
-                    help="tensor list: llama-3-8b (int8 rho, the headline) or llama-1.1b (int16 rho)")
+    ap.add_argument("--workload", default=W.LLAMA3_8B.name, choices=sorted(WORKLOADS) + [SINGLE],
+                    help="tensor list: llama-3-8b (int8 rho, the headline) or llama-1.1b (int16 rho); "
+                         f"{SINGLE}: the single 65,553-parameter tensor (latency-bound, parity-test size)")
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -651,6 +698,14 @@ def main():
                          "ablation format (parameter: bf16_rho8, bf16_rho16, bf16, f32; states: companded, "
                          "linear, f32) instead of the fast step")
     args = ap.parse_args()
+    if args.workload == SINGLE:
+        if args.impl != "gb300":
+            raise SystemExit("the single-tensor workload has no reference arm")
+        import quantized_state_optimizer_gb300 as fo
+        fo.lib()
+        torch.cuda.set_device(0)
+        print(json.dumps(single_tensor_line(args.steps, args.warmup, torch.device("cuda", 0))), flush=True)
+        return
     use_workload(args.workload)
     ws, rank, local = dist_env()
     numels = [s.numel for s in W.llama_tensor_list(MODEL)]
@@ -753,7 +808,8 @@ def main():
     cfg["hbm_gbs"] = achieved
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": statistics.median(per),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
